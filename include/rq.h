@@ -1,0 +1,149 @@
+/*
+ * librq -- ResidualQuant decode attention over a residual-quantised per-loop KV cache,
+ * native to GB300 (sm_103a).  Plain C ABI: device pointers, sizes, a stream handle.
+ *
+ * The method ("ResidualQuant: KV Cache Quantization for Looped Transformers with 2-Bit
+ * Residuals", abstract; rit.work summary, "How each pass's KV cache is reconstructed"):
+ * a looped Transformer applies one block L times per token and every loop (pass) makes
+ * its own K/V.  For each token, the FINAL loop's K/V is stored as the reference in
+ * asymmetric INT4; every other loop l is stored as a residual against the scaled
+ * reference,
+ *     x_l  ~=  a_l * ref_hat + R^T * deq(res_l),
+ * where a_l is the least-squares scale <x_l, ref_hat> / <ref_hat, ref_hat>, R is an
+ * orthogonal channel rotation per (layer, kv-head, K/V) and res_l is an asymmetric
+ * INT2 (or INT4: loop-wise mixed precision) code of R (x_l - a_l ref_hat).  The current
+ * token stays in BF16 until its final loop ends (deferred write); then all its loops are
+ * encoded and appended.  Decode attention rebuilds reference and residuals inside the
+ * attention computation and never writes decompressed K/V to memory.
+ *
+ * Conventions for every entry point
+ *   - All tensors are caller-owned device memory (except rq_shape / rq_cache structs,
+ *     which are host memory read during the call).  The library never allocates, frees
+ *     or synchronises; all work is enqueued on `stream` (a cudaStream_t, 0 = legacy
+ *     default stream) of the current device.
+ *   - fp16 and bf16 tensors are passed as uint16_t pointers holding the raw bits.
+ *   - Arguments are validated before anything is enqueued: an invalid call returns a
+ *     status and enqueues nothing.  A failed launch returns RQ_ERR_CUDA.  No C++
+ *     exception crosses the ABI and the library keeps no mutable global state.
+ *
+ * Packed cache layout (one layer; kv = 0 for K, 1 for V; d = head_dim, ng = d / 32):
+ *   ref_codes[kv]     uint8  [B][Hkv][cap][d/2]          INT4 reference codes
+ *   ref_meta[kv]      fp16   [B][Hkv][cap][ng][2]        per group (step, offset)
+ *   res_codes[kv][l]  uint8  [B][Hkv][cap][d*b_l/8]      residual codes, l < L-1
+ *   res_meta[kv][l]   fp16   [B][Hkv][cap][ng][2]
+ *   alpha[kv][l]      fp16   [B][Hkv][cap]               least-squares scale a_l
+ *   rot_signs[kv]     int8   [Hkv][d]                    +-1; R = H_d diag(signs)/sqrt(d)
+ * A token's code row packs channel i into byte i*b/8 at bit offset (i*b) % 8.  K rows
+ * are stored one after another.  V rows are stored in token pairs: for tokens 2p and
+ * 2p+1 the 16-bit units of the two rows alternate (unit u of token 2p, unit u of token
+ * 2p+1, unit u+1 of token 2p, ...), so capacity must be even.  Groups are 32 contiguous
+ * channels: original channels for the reference, rotated channels for residuals.
+ */
+#ifndef RQ_H_
+#define RQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RQ_MAX_LOOPS 16
+
+typedef enum {
+  RQ_OK = 0,
+  RQ_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, range out of bounds   */
+  RQ_ERR_UNSUPPORTED = 2, /* head_dim not 64/128, group not 32, bits not 2/4, ...    */
+  RQ_ERR_WORKSPACE = 3,   /* workspace missing or smaller than rq_decode_workspace_bytes */
+  RQ_ERR_CUDA = 4,        /* a CUDA call or kernel launch failed                     */
+  RQ_ERR_INTERNAL = 5
+} rq_status;
+
+typedef struct {
+  int32_t batch;        /* B                                                          */
+  int32_t n_q_heads;    /* Hq, a multiple of n_kv_heads (GQA: query head h reads       */
+  int32_t n_kv_heads;   /*     kv-head h / (Hq / Hkv))                                 */
+  int32_t head_dim;     /* d: 64 or 128                                               */
+  int32_t n_loops;      /* L: 1..16; loop L-1 is the reference                         */
+  int32_t group;        /* must be 32                                                  */
+  int32_t capacity;     /* tokens per (sequence, kv-head) slot in the cache; even      */
+  int8_t res_bits[RQ_MAX_LOOPS]; /* residual bits of loop l < L-1: 2 or 4              */
+  float softmax_scale;  /* 0 => 1/sqrt(d)                                              */
+} rq_shape;
+
+typedef struct {
+  uint8_t* ref_codes[2];
+  uint16_t* ref_meta[2];
+  uint8_t* res_codes[2][RQ_MAX_LOOPS];
+  uint16_t* res_meta[2][RQ_MAX_LOOPS];
+  uint16_t* alpha[2][RQ_MAX_LOOPS];
+  const int8_t* rot_signs[2];
+} rq_cache;
+
+/* Bytes of one layer's packed cache (K and V, all arrays above except rot_signs):
+ * per token-head and K/V, d/2 + 4*ng for the reference plus d*b_l/8 + 4*ng + 2 per
+ * non-final loop.  Returns 0 for an invalid shape. */
+size_t rq_cache_bytes(const rq_shape* shape);
+
+/* Deferred write (rit.work summary, "How each pass's KV cache is reconstructed": the
+ * current token's loop states stay in BF16 until the final loop ends, then the
+ * compressed cache is written).  Encodes n_new tokens per sequence, all L loops, K and V,
+ * every kv-head, and stores them at their cache positions.
+ *   kv_new     bf16 element (b, j, kv, l, h, i) at
+ *              b*strides[0] + j*strides[1] + kv*strides[2] + l*strides[3] + h*strides[4] + i
+ *              (channel stride 1; strides in elements, non-negative)
+ *   positions  device int32 [B][n_new]: cache slot of new token j of sequence b; or NULL,
+ *              in which case slot = pos_begin + j.  Slots must lie in [0, capacity): a
+ *              device-side slot outside that range is skipped (nothing written).
+ *   n_new      >= 0 (0: nothing enqueued).
+ * The same slot must not be written twice in one call.  Codes, step/offset and a_l follow
+ * the header comment's layout; rounding is to nearest even throughout. */
+rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache,
+                           const uint16_t* kv_new, const int64_t strides[5],
+                           const int32_t* positions, int32_t pos_begin, int32_t n_new,
+                           void* stream);
+
+/* Workspace bytes needed by rq_decode_attention / rq_bf16_decode_attention for this
+ * shape, loop_count and max_ctx on the current device (split-KV partials). */
+size_t rq_decode_workspace_bytes(const rq_shape* shape, int32_t loop_count, int32_t max_ctx);
+
+/* Fused decode attention over the packed cache (rit.work summary, "How each pass's KV
+ * cache is reconstructed": reference and residuals are rebuilt in small blocks inside
+ * attention, no decompressed K/V is written back).
+ *   q          bf16 [B][Hq][loop_count][d]: the queries of loops loop_begin..+loop_count-1
+ *   loop_begin, loop_count: 0 <= loop_begin, loop_begin + loop_count <= L, loop_count >= 1.
+ *              loop_count = 1 is the causal per-loop call of a real decode step;
+ *              loop_count = L supplies all loops' queries at once (the reference tile is
+ *              then read once for all loops).
+ *   pending_kv bf16 [B][2][loop_count][Hkv][d] (0 = K, 1 = V): the current token's BF16
+ *              state of each loop in the call, attended after the cached tokens; or NULL.
+ *   ctx_lens   device int32 [B]: cached tokens of each sequence (slots 0..ctx_len-1).
+ *   max_ctx    host upper bound of ctx_lens (<= capacity); sizes the split-KV grid.
+ *   out        bf16 [B][Hq][loop_count][d].  A row with no cached and no pending token
+ *              is written as zeros.
+ *   ws         device workspace of at least rq_decode_workspace_bytes(...) bytes.
+ * Loop-l queries attend over loop l's rebuilt K/V; scores are scaled by softmax_scale. */
+rq_status rq_decode_attention(const rq_shape* shape, const rq_cache* cache,
+                              const uint16_t* q, int32_t loop_begin, int32_t loop_count,
+                              const uint16_t* pending_kv, const int32_t* ctx_lens,
+                              int32_t max_ctx, uint16_t* out, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* Comparison kernel: the same decode attention over an uncompressed BF16 cache,
+ *   k, v  bf16 [B][Hkv][L][capacity][d]
+ * with every other argument as in rq_decode_attention. */
+rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k,
+                                   const uint16_t* v, const uint16_t* q, int32_t loop_begin,
+                                   int32_t loop_count, const uint16_t* pending_kv,
+                                   const int32_t* ctx_lens, int32_t max_ctx, uint16_t* out,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/* Human-readable name of a status. */
+const char* rq_status_str(rq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RQ_H_ */

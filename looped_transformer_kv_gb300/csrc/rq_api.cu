@@ -1,0 +1,147 @@
+// C ABI of librq: argument validation, then the internal launchers.  Nothing is
+// enqueued unless every check passes; no exception crosses this boundary.
+#include <cmath>
+#include <new>
+
+#include "rq_common.cuh"
+#include "rq_kernels.h"
+
+namespace {
+
+rq_status check_shape(const rq_shape* s) {
+  if (!s) return RQ_ERR_INVALID_ARG;
+  if (s->batch <= 0 || s->n_q_heads <= 0 || s->n_kv_heads <= 0 || s->capacity <= 0 ||
+      s->n_loops <= 0)
+    return RQ_ERR_INVALID_ARG;
+  if (s->n_q_heads % s->n_kv_heads != 0) return RQ_ERR_INVALID_ARG;
+  if (s->capacity % 2 != 0) return RQ_ERR_INVALID_ARG;
+  if (s->group != 32) return RQ_ERR_UNSUPPORTED;
+  if (s->head_dim != 64 && s->head_dim != 128) return RQ_ERR_UNSUPPORTED;
+  if (s->n_loops > RQ_MAX_LOOPS) return RQ_ERR_UNSUPPORTED;
+  if (s->batch > 65535 || s->n_kv_heads > 65535) return RQ_ERR_UNSUPPORTED;
+  for (int l = 0; l < s->n_loops - 1; ++l)
+    if (s->res_bits[l] != 2 && s->res_bits[l] != 4) return RQ_ERR_UNSUPPORTED;
+  if (!(s->softmax_scale >= 0.f) || std::isinf(s->softmax_scale)) return RQ_ERR_INVALID_ARG;
+  return RQ_OK;
+}
+
+rq_status check_cache(const rq_shape* s, const rq_cache* c) {
+  if (!c) return RQ_ERR_INVALID_ARG;
+  for (int kv = 0; kv < 2; ++kv) {
+    if (!c->ref_codes[kv] || !c->ref_meta[kv] || !c->rot_signs[kv]) return RQ_ERR_INVALID_ARG;
+    for (int l = 0; l < s->n_loops - 1; ++l)
+      if (!c->res_codes[kv][l] || !c->res_meta[kv][l] || !c->alpha[kv][l])
+        return RQ_ERR_INVALID_ARG;
+  }
+  return RQ_OK;
+}
+
+rq_status check_decode(const rq_shape* s, const uint16_t* q, int32_t loop_begin,
+                       int32_t loop_count, const int32_t* ctx_lens, int32_t max_ctx,
+                       uint16_t* out, void* ws, size_t ws_bytes) {
+  if (!q || !ctx_lens || !out) return RQ_ERR_INVALID_ARG;
+  if (loop_count < 1 || loop_begin < 0 || loop_begin + loop_count > s->n_loops)
+    return RQ_ERR_INVALID_ARG;
+  if (max_ctx < 0 || max_ctx > s->capacity) return RQ_ERR_INVALID_ARG;
+  if (int64_t(s->batch) * s->n_q_heads * loop_count > (int64_t(1) << 31))
+    return RQ_ERR_UNSUPPORTED;
+  const size_t need = rq_decode_workspace_bytes(s, loop_count, max_ctx);
+  if (!ws || ws_bytes < need) return RQ_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 15) != 0) return RQ_ERR_WORKSPACE;
+  return RQ_OK;
+}
+
+rq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t rq_cache_bytes(const rq_shape* s) {
+  if (check_shape(s) != RQ_OK) return 0;
+  const size_t d = size_t(s->head_dim), ng = d / 32;
+  size_t per = d / 2 + 4 * ng;
+  for (int l = 0; l < s->n_loops - 1; ++l) per += d * size_t(s->res_bits[l]) / 8 + 4 * ng + 2;
+  return 2 * per * size_t(s->capacity) * size_t(s->n_kv_heads) * size_t(s->batch);
+}
+
+rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache, const uint16_t* kv_new,
+                           const int64_t strides[5], const int32_t* positions, int32_t pos_begin,
+                           int32_t n_new, void* stream) {
+  rq_status st = check_shape(shape);
+  if (st != RQ_OK) return st;
+  if ((st = check_cache(shape, cache)) != RQ_OK) return st;
+  if (!kv_new || !strides || n_new < 0) return RQ_ERR_INVALID_ARG;
+  for (int k = 0; k < 5; ++k)
+    if (strides[k] < 0) return RQ_ERR_INVALID_ARG;
+  if (!positions && (pos_begin < 0 || int64_t(pos_begin) + n_new > shape->capacity))
+    return RQ_ERR_INVALID_ARG;
+  if (n_new == 0) return RQ_OK;
+  try {
+    return from_cuda(rq::launch_encode(*shape, *cache, kv_new, strides, positions, pos_begin,
+                                       n_new, static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return RQ_ERR_INTERNAL;
+  }
+}
+
+size_t rq_decode_workspace_bytes(const rq_shape* s, int32_t loop_count, int32_t max_ctx) {
+  if (check_shape(s) != RQ_OK || loop_count < 1 || max_ctx < 0) return 0;
+  const rq::SplitPlan p = rq::plan_splits(*s, loop_count, max_ctx);
+  return size_t(s->batch) * s->n_q_heads * loop_count * p.n_splits * rq::partial_floats(*s) *
+         sizeof(float);
+}
+
+rq_status rq_decode_attention(const rq_shape* shape, const rq_cache* cache, const uint16_t* q,
+                              int32_t loop_begin, int32_t loop_count, const uint16_t* pending_kv,
+                              const int32_t* ctx_lens, int32_t max_ctx, uint16_t* out, void* ws,
+                              size_t ws_bytes, void* stream) {
+  rq_status st = check_shape(shape);
+  if (st != RQ_OK) return st;
+  if ((st = check_cache(shape, cache)) != RQ_OK) return st;
+  if ((st = check_decode(shape, q, loop_begin, loop_count, ctx_lens, max_ctx, out, ws,
+                         ws_bytes)) != RQ_OK)
+    return st;
+  try {
+    return from_cuda(rq::launch_rq_decode(*shape, *cache, q, loop_begin, loop_count, pending_kv,
+                                          ctx_lens, max_ctx, out, static_cast<float*>(ws),
+                                          static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return RQ_ERR_INTERNAL;
+  }
+}
+
+rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k, const uint16_t* v,
+                                   const uint16_t* q, int32_t loop_begin, int32_t loop_count,
+                                   const uint16_t* pending_kv, const int32_t* ctx_lens,
+                                   int32_t max_ctx, uint16_t* out, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  rq_status st = check_shape(shape);
+  if (st != RQ_OK) return st;
+  if (!k || !v) return RQ_ERR_INVALID_ARG;
+  if (shape->n_q_heads / shape->n_kv_heads > 8) return RQ_ERR_UNSUPPORTED;
+  if ((st = check_decode(shape, q, loop_begin, loop_count, ctx_lens, max_ctx, out, ws,
+                         ws_bytes)) != RQ_OK)
+    return st;
+  try {
+    return from_cuda(rq::launch_bf16_decode(*shape, k, v, q, loop_begin, loop_count, pending_kv,
+                                            ctx_lens, max_ctx, out, static_cast<float*>(ws),
+                                            static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return RQ_ERR_INTERNAL;
+  }
+}
+
+const char* rq_status_str(rq_status s) {
+  switch (s) {
+    case RQ_OK: return "RQ_OK";
+    case RQ_ERR_INVALID_ARG: return "RQ_ERR_INVALID_ARG";
+    case RQ_ERR_UNSUPPORTED: return "RQ_ERR_UNSUPPORTED";
+    case RQ_ERR_WORKSPACE: return "RQ_ERR_WORKSPACE";
+    case RQ_ERR_CUDA: return "RQ_ERR_CUDA";
+    case RQ_ERR_INTERNAL: return "RQ_ERR_INTERNAL";
+  }
+  return "RQ_ERR_UNKNOWN";
+}
+
+}  // extern "C"

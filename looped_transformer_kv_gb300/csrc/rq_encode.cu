@@ -1,0 +1,218 @@
+// ResidualQuant encode: runs once the token's final loop has finished (deferred write,
+// rit.work summary "How each pass's KV cache is reconstructed").  One warp encodes one
+// (sequence, new token, kv-head, K/V): the final loop's state becomes the INT4 reference,
+// every other loop a least-squares-scaled, Hadamard-rotated 2- or 4-bit residual.
+#include "rq_common.cuh"
+#include "rq_kernels.h"
+
+namespace rq {
+namespace {
+
+struct EncodeArgs {
+  rq_cache cache;
+  const uint16_t* kv_new;
+  int64_t sb, st, skv, sl, sh;  // element strides of kv_new
+  const int32_t* positions;
+  int32_t pos_begin;
+  int32_t n_new;
+  int32_t B, H, L, cap;
+  int8_t res_bits[RQ_MAX_LOOPS];
+};
+
+// Group min / max over the lanes that share a 32-channel group (LPG lanes).
+template <int LPG>
+__device__ __forceinline__ void group_minmax(float& mn, float& mx) {
+#pragma unroll
+  for (int o = 1; o < LPG; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(RQ_FULL_MASK, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(RQ_FULL_MASK, mx, o));
+  }
+}
+
+// Quantise the P channels this lane holds with (step, offset) from the group's min/max;
+// returns the codes, writes the dequantised values into deq and the fp16 pair into s_h/z_h.
+template <int P, int LEVELS>
+__device__ __forceinline__ void quantize_lane(const float (&v)[P], int (&c)[P], float (&deq)[P],
+                                              uint16_t& s_bits, uint16_t& z_bits) {
+  constexpr int LPG = kGroup / P;
+  float mn = v[0], mx = v[0];
+#pragma unroll
+  for (int j = 1; j < P; ++j) {
+    mn = fminf(mn, v[j]);
+    mx = fmaxf(mx, v[j]);
+  }
+  group_minmax<LPG>(mn, mx);
+  const float s = __fdiv_rn(__fsub_rn(mx, mn), float(LEVELS));
+  s_bits = float_to_half_bits(s);
+  z_bits = float_to_half_bits(mn);
+  const float s_h = half_bits_to_float(s_bits);
+  const float z_h = half_bits_to_float(z_bits);
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    int code = 0;
+    if (s_h > 0.0f) {
+      float qv = rintf(__fdiv_rn(__fsub_rn(v[j], z_h), s_h));
+      qv = fminf(fmaxf(qv, 0.0f), float(LEVELS));
+      code = int(qv);
+    }
+    c[j] = code;
+    deq[j] = fmaf(float(code), s_h, z_h);
+  }
+}
+
+// Store the packed bits of this lane's P channels.  BITS*P bits per lane: 4 (d 64, 2-bit),
+// 8 or 16.  Row byte k = lane's byte index; V rows go to the token-pair layout.
+template <int P, int BITS>
+__device__ __forceinline__ void store_codes(uint8_t* slot, int64_t tok, int row_bytes, bool is_v,
+                                            const int (&c)[P], int lane) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < P; ++j) w |= uint32_t(c[j]) << (BITS * j);
+  constexpr int LANE_BITS = BITS * P;
+  if (LANE_BITS == 4) {
+    uint32_t other = __shfl_down_sync(RQ_FULL_MASK, w, 1);
+    if ((lane & 1) == 0) {
+      const int k = lane >> 1;
+      uint8_t byte = uint8_t(w | (other << 4));
+      int64_t off = is_v ? vpair_offset(tok, k, row_bytes) : tok * row_bytes + k;
+      slot[off] = byte;
+    }
+  } else if (LANE_BITS == 8) {
+    const int k = lane;
+    int64_t off = is_v ? vpair_offset(tok, k, row_bytes) : tok * row_bytes + k;
+    slot[off] = uint8_t(w);
+  } else {  // 16 bits: one aligned 16-bit unit
+    const int k = 2 * lane;
+    int64_t off = is_v ? vpair_offset(tok, k, row_bytes) : tok * row_bytes + k;
+    *reinterpret_cast<uint16_t*>(slot + off) = uint16_t(w);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
+  constexpr int P = D / 32;   // channels per lane
+  constexpr int LPG = kGroup / P;
+  constexpr int NG = D / kGroup;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t total = int64_t(a.B) * a.n_new * a.H * 2;
+  if (wid >= total) return;
+  int64_t r = wid;
+  const int kv = int(r % 2); r /= 2;
+  const int h = int(r % a.H); r /= a.H;
+  const int j = int(r % a.n_new); r /= a.n_new;
+  const int b = int(r);
+  const int pos = a.positions ? a.positions[int64_t(b) * a.n_new + j] : a.pos_begin + j;
+  if (pos < 0 || pos >= a.cap) return;
+  const bool is_v = kv == 1;
+  const int64_t slot_tok = int64_t(b) * a.H + h;        // (b, h) slot index
+  const int64_t tok = pos;
+
+  const uint16_t* src = a.kv_new + int64_t(b) * a.sb + int64_t(j) * a.st + int64_t(kv) * a.skv +
+                        int64_t(h) * a.sh + lane * P;
+  const int L = a.L;
+  auto load = [&](int l, float (&v)[P]) {
+    const uint16_t* p = src + int64_t(l) * a.sl;
+#pragma unroll
+    for (int q = 0; q < P; ++q) v[q] = bf16_bits_to_float(p[q]);
+  };
+
+  // ---- reference: the final loop, INT4 ----
+  float x_ref[P], ref_hat[P];
+  int c[P];
+  load(L - 1, x_ref);
+  uint16_t s_bits, z_bits;
+  quantize_lane<P, 15>(x_ref, c, ref_hat, s_bits, z_bits);
+  {
+    uint8_t* codes = a.cache.ref_codes[kv] + slot_tok * int64_t(a.cap) * (D / 2);
+    store_codes<P, 4>(codes, tok, D / 2, is_v, c, lane);
+    if (lane % LPG == 0) {
+      const int g = lane / LPG;
+      uint16_t* meta = a.cache.ref_meta[kv] + (slot_tok * a.cap + tok) * (2 * NG) + 2 * g;
+      *reinterpret_cast<uint32_t*>(meta) = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
+    }
+  }
+  // <ref_hat, ref_hat> is shared by all loops
+  float den = 0.f;
+#pragma unroll
+  for (int q = 0; q < P; ++q) den = fmaf(ref_hat[q], ref_hat[q], den);
+  den = warp_sum(den);
+
+  float sgn[P];
+  {
+    const int8_t* sp = a.cache.rot_signs[kv] + int64_t(h) * D + lane * P;
+#pragma unroll
+    for (int q = 0; q < P; ++q) sgn[q] = float(sp[q]);
+  }
+  const float inv_sqrt_d = (D == 128) ? 0.08838834764831845f : 0.125f;
+
+  for (int l = 0; l < L - 1; ++l) {
+    float x[P];
+    load(l, x);
+    // least-squares scale against the dequantised reference
+    float num = 0.f;
+#pragma unroll
+    for (int q = 0; q < P; ++q) num = fmaf(x[q], ref_hat[q], num);
+    num = warp_sum(num);
+    const float alpha = den > 0.f ? __fdiv_rn(num, den) : 0.f;
+    const uint16_t a_bits = float_to_half_bits(alpha);
+    const float a_h = half_bits_to_float(a_bits);
+    if (lane == 0) a.cache.alpha[kv][l][slot_tok * a.cap + tok] = a_bits;
+    // residual, rotation R r = H (signs * r) / sqrt(d)
+    float y[P];
+#pragma unroll
+    for (int q = 0; q < P; ++q) y[q] = fmaf(-a_h, ref_hat[q], x[q]) * sgn[q];
+    warp_fwht<P>(y, lane);
+#pragma unroll
+    for (int q = 0; q < P; ++q) y[q] *= inv_sqrt_d;
+    float deq[P];
+    const int bits = a.res_bits[l];
+    const int row = D * bits / 8;
+    uint8_t* codes = a.cache.res_codes[kv][l] + slot_tok * int64_t(a.cap) * row;
+    if (bits == 2) {
+      quantize_lane<P, 3>(y, c, deq, s_bits, z_bits);
+      store_codes<P, 2>(codes, tok, row, is_v, c, lane);
+    } else {
+      quantize_lane<P, 15>(y, c, deq, s_bits, z_bits);
+      store_codes<P, 4>(codes, tok, row, is_v, c, lane);
+    }
+    if (lane % LPG == 0) {
+      const int g = lane / LPG;
+      uint16_t* meta = a.cache.res_meta[kv][l] + (slot_tok * a.cap + tok) * (2 * NG) + 2 * g;
+      *reinterpret_cast<uint32_t*>(meta) = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const uint16_t* kv_new,
+                          const int64_t strides[5], const int32_t* positions, int32_t pos_begin,
+                          int32_t n_new, cudaStream_t stream) {
+  EncodeArgs a;
+  a.cache = cache;
+  a.kv_new = kv_new;
+  a.sb = strides[0];
+  a.st = strides[1];
+  a.skv = strides[2];
+  a.sl = strides[3];
+  a.sh = strides[4];
+  a.positions = positions;
+  a.pos_begin = pos_begin;
+  a.n_new = n_new;
+  a.B = s.batch;
+  a.H = s.n_kv_heads;
+  a.L = s.n_loops;
+  a.cap = s.capacity;
+  for (int l = 0; l < RQ_MAX_LOOPS; ++l) a.res_bits[l] = s.res_bits[l];
+  const int64_t warps = int64_t(s.batch) * n_new * s.n_kv_heads * 2;
+  const int64_t blocks = (warps + 3) / 4;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (s.head_dim == 128)
+    encode_kernel<128><<<unsigned(blocks), 128, 0, stream>>>(a);
+  else
+    encode_kernel<64><<<unsigned(blocks), 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace rq

@@ -1,0 +1,138 @@
+"""Thin PyTorch binding of librq: argument marshalling only.
+
+Every step of encode and decode attention runs in the library's CUDA kernels; PyTorch
+provides device memory and the current stream.  Names follow the C ABI (include/rq.h).
+"""
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import RQ_MAX_LOOPS, RqCache, RqShape, RqSynthParams, check
+
+GROUP = 32
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_shape(batch, n_q_heads, n_kv_heads, head_dim, n_loops, capacity, res_bits,
+               softmax_scale=0.0, group=GROUP):
+    """rq_shape for one layer; res_bits lists the residual bits of loops 0..L-2."""
+    s = RqShape()
+    s.batch, s.n_q_heads, s.n_kv_heads = batch, n_q_heads, n_kv_heads
+    s.head_dim, s.n_loops, s.group, s.capacity = head_dim, n_loops, group, capacity
+    for l, b in enumerate(res_bits):
+        s.res_bits[l] = int(b)
+    s.softmax_scale = float(softmax_scale)
+    return s
+
+
+def res_bits_of(shape):
+    return [int(shape.res_bits[l]) for l in range(shape.n_loops - 1)]
+
+
+class PackedCache:
+    """Device arrays of one layer's packed cache (layout of include/rq.h) + rotation signs."""
+
+    def __init__(self, shape, rot_signs, device="cuda"):
+        B, H, cap, d = shape.batch, shape.n_kv_heads, shape.capacity, shape.head_dim
+        ng = d // GROUP
+        u8, f16 = torch.uint8, torch.float16
+        self.shape = shape
+        self.ref_codes = [torch.empty(B, H, cap, d // 2, dtype=u8, device=device) for _ in range(2)]
+        self.ref_meta = [torch.empty(B, H, cap, ng, 2, dtype=f16, device=device) for _ in range(2)]
+        self.res_codes = [[], []]
+        self.res_meta = [[], []]
+        self.alpha = [[], []]
+        for kv in range(2):
+            for b in res_bits_of(shape):
+                self.res_codes[kv].append(torch.empty(B, H, cap, d * b // 8, dtype=u8, device=device))
+                self.res_meta[kv].append(torch.empty(B, H, cap, ng, 2, dtype=f16, device=device))
+                self.alpha[kv].append(torch.empty(B, H, cap, dtype=f16, device=device))
+        self.rot_signs = rot_signs.to(device=device, dtype=torch.int8).contiguous()  # [2][H][d]
+        assert tuple(self.rot_signs.shape) == (2, H, d)
+        c = RqCache()
+        for kv in range(2):
+            c.ref_codes[kv] = self.ref_codes[kv].data_ptr()
+            c.ref_meta[kv] = self.ref_meta[kv].data_ptr()
+            c.rot_signs[kv] = self.rot_signs[kv].data_ptr()
+            for l in range(shape.n_loops - 1):
+                c.res_codes[kv][l] = self.res_codes[kv][l].data_ptr()
+                c.res_meta[kv][l] = self.res_meta[kv][l].data_ptr()
+                c.alpha[kv][l] = self.alpha[kv][l].data_ptr()
+        self.struct = c
+
+    def tensors(self):
+        out = list(self.ref_codes) + list(self.ref_meta)
+        for kv in range(2):
+            out += self.res_codes[kv] + self.res_meta[kv] + self.alpha[kv]
+        return out
+
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in self.tensors())
+
+
+def cache_bytes(shape):
+    return int(_lib.lib().rq_cache_bytes(ctypes.byref(shape)))
+
+
+def encode_append(shape, cache, kv_new, positions=None, pos_begin=0, stream=None):
+    """kv_new: bf16 [B][n_new][2][L][Hkv][d] (any strides, channel stride 1)."""
+    assert kv_new.dtype == torch.bfloat16 and kv_new.dim() == 6 and kv_new.stride(5) == 1
+    st = (ctypes.c_int64 * 5)(*[kv_new.stride(i) for i in range(5)])
+    n_new = kv_new.shape[1]
+    check("rq_encode_append", _lib.lib().rq_encode_append(
+        ctypes.byref(shape), ctypes.byref(cache.struct), _ptr(kv_new), st, _ptr(positions),
+        int(pos_begin), int(n_new), _stream(stream)))
+
+
+def decode_workspace_bytes(shape, loop_count, max_ctx):
+    return int(_lib.lib().rq_decode_workspace_bytes(ctypes.byref(shape), int(loop_count),
+                                                    int(max_ctx)))
+
+
+def decode_attention(shape, cache, q, loop_begin, loop_count, pending_kv, ctx_lens, max_ctx,
+                     out, ws, stream=None):
+    check("rq_decode_attention", _lib.lib().rq_decode_attention(
+        ctypes.byref(shape), ctypes.byref(cache.struct), _ptr(q), int(loop_begin),
+        int(loop_count), _ptr(pending_kv), _ptr(ctx_lens), int(max_ctx), _ptr(out), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def bf16_decode_attention(shape, k, v, q, loop_begin, loop_count, pending_kv, ctx_lens, max_ctx,
+                          out, ws, stream=None):
+    check("rq_bf16_decode_attention", _lib.lib().rq_bf16_decode_attention(
+        ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(q), int(loop_begin), int(loop_count),
+        _ptr(pending_kv), _ptr(ctx_lens), int(max_ctx), _ptr(out), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def synth_params(seed, layer, head_dim, n_kv_heads, dist, sigma, outlier_mult, outlier_table):
+    """rq_synth_params; outlier_table: device int32 [Hkv][2][n] (kept alive by the caller)."""
+    p = RqSynthParams()
+    p.seed, p.layer, p.head_dim, p.n_kv_heads, p.dist = seed, layer, head_dim, n_kv_heads, dist
+    for l, s in enumerate(sigma):
+        p.sigma[l] = float(s)
+    p.outlier_mult = float(outlier_mult)
+    p.n_outliers = int(outlier_table.shape[-1]) if outlier_table is not None else 0
+    p.outlier_table = outlier_table.data_ptr() if outlier_table is not None else None
+    return p
+
+
+def synth_states(params, out, strides, b0, nb, t0, nt, l0, nl, stream=None):
+    st = (ctypes.c_int64 * 5)(*strides)
+    check("rq_synth_states", _lib.lib().rq_synth_states(
+        ctypes.byref(params), _ptr(out), st, b0, nb, t0, nt, l0, nl, _stream(stream)))
+
+
+def synth_queries(params, out, n_q_heads, b0, nb, l0, nl, step=0, stream=None):
+    check("rq_synth_queries", _lib.lib().rq_synth_queries(
+        ctypes.byref(params), _ptr(out), n_q_heads, b0, nb, l0, nl, step, _stream(stream)))

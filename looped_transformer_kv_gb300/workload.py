@@ -1,0 +1,155 @@
+"""Device-resident synthetic workloads: packed cache, BF16 cache, queries, pending tokens.
+
+Inputs come from the seeded generator (the `synth` package's recipe, run on the GPU by
+librq's synthetic-input kernel), then the packed cache is built by librq's encode
+(bulk deferred write of positions 0..capacity-1, in token chunks so that no full BF16 copy
+of the cache is needed).
+"""
+
+import numpy as np
+import torch
+
+import synth
+
+from . import rq
+
+
+class Workload:
+    def __init__(self, cfg, layer=0, capacity=None, ctx_lens=None, build_rq=True,
+                 build_bf16=False, chunk_tokens=2048, device="cuda", batch=None):
+        self.cfg = cfg
+        self.layer = layer
+        self.device = device
+        B = cfg.batch if batch is None else batch
+        H, Hq, d, L = cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim, cfg.n_loops
+        cap = cfg.ctx if capacity is None else capacity
+        cap += cap % 2
+        self.B, self.H, self.Hq, self.d, self.L, self.cap = B, H, Hq, d, L, cap
+        if ctx_lens is None:
+            ctx_lens = [min(cfg.ctx, cap)] * B
+        self.ctx_list = [int(c) for c in ctx_lens]
+        assert len(self.ctx_list) == B and all(0 <= c <= cap for c in self.ctx_list)
+        self.max_ctx = max(self.ctx_list) if B else 0
+        self.ctx_lens = torch.tensor(self.ctx_list, dtype=torch.int32, device=device)
+        self.shape = rq.make_shape(B, Hq, H, d, L, cap, cfg.res_bits[: L - 1])
+        signs = synth.rotation_signs(cfg, layer)                      # [H][2][d]
+        self.signs_np = signs
+        self.outliers = torch.from_numpy(synth.outlier_table(cfg, layer)).to(device)
+        self.params = rq.synth_params(cfg.seed, layer, d, H, cfg.dist, cfg.sigma,
+                                      cfg.outlier_mult, self.outliers if cfg.n_outliers else None)
+        self.cache = None
+        if build_rq:
+            self.cache = rq.PackedCache(self.shape, torch.from_numpy(signs.transpose(1, 0, 2).copy()),
+                                        device=device)
+            self._build_rq(chunk_tokens)
+        self.k = self.v = None
+        if build_bf16:
+            self._build_bf16()
+        # queries [B][Hq][L][d] and the pending (current) token at position ctx_len[b]
+        self.q = torch.empty(B, Hq, L, d, dtype=torch.bfloat16, device=device)
+        rq.synth_queries(self.params, self.q, Hq, 0, B, 0, L)
+        self.pending = torch.empty(B, 2, L, H, d, dtype=torch.bfloat16, device=device)
+        st = self.pending.stride()
+        for b in range(B):
+            rq.synth_states(self.params, self.pending[b], (0, 0, st[1], st[2], st[3]),
+                            b, 1, self.ctx_list[b], 1, 0, L)
+        self.q_loop = [self.q[:, :, l:l + 1].contiguous() for l in range(L)]
+        self.pending_loop = [self.pending[:, :, l:l + 1].contiguous() for l in range(L)]
+
+    # ------------------------------------------------------------------ builders
+    def _build_rq(self, chunk_tokens):
+        B, H, d, L, cap = self.B, self.H, self.d, self.L, self.cap
+        bmax = max(1, min(B, (1 << 28) // max(1, chunk_tokens * 2 * L * H * d)))
+        buf = torch.empty(bmax, chunk_tokens, 2, L, H, d, dtype=torch.bfloat16, device=self.device)
+        st = buf.stride()
+        for b0 in range(0, B, bmax):
+            nb = min(bmax, B - b0)
+            for t0 in range(0, cap, chunk_tokens):
+                nt = min(chunk_tokens, cap - t0)
+                rq.synth_states(self.params, buf, st[:5], b0, nb, t0, nt, 0, L)
+                view = buf[:nb, :nt]
+                sub = rq.make_shape(nb, self.Hq, H, d, L, cap, self.cfg.res_bits[: L - 1])
+                sub_cache = self._sub_cache(b0, nb)
+                rq.encode_append(sub, sub_cache, view, pos_begin=t0)
+        del buf
+
+    def _sub_cache(self, b0, nb):
+        """A view of the cache restricted to sequences [b0, b0+nb) (pointer offsets)."""
+        c = rq._lib.RqCache()
+        full = self.cache
+        for kv in range(2):
+            c.ref_codes[kv] = full.ref_codes[kv][b0].data_ptr()
+            c.ref_meta[kv] = full.ref_meta[kv][b0].data_ptr()
+            c.rot_signs[kv] = full.rot_signs[kv].data_ptr()
+            for l in range(self.L - 1):
+                c.res_codes[kv][l] = full.res_codes[kv][l][b0].data_ptr()
+                c.res_meta[kv][l] = full.res_meta[kv][l][b0].data_ptr()
+                c.alpha[kv][l] = full.alpha[kv][l][b0].data_ptr()
+
+        class _V:
+            pass
+
+        v = _V()
+        v.struct = c
+        return v
+
+    def _build_bf16(self):
+        B, H, d, L, cap = self.B, self.H, self.d, self.L, self.cap
+        kv = torch.empty(2, B, H, L, cap, d, dtype=torch.bfloat16, device=self.device)
+        s = kv.stride()                      # (kv, b, h, l, t, i)
+        rq.synth_states(self.params, kv, (s[1], s[4], s[0], s[3], s[2]), 0, B, 0, cap, 0, L)
+        self.kv_bf16 = kv
+        self.k, self.v = kv[0], kv[1]
+
+    # ------------------------------------------------------------------ calls
+    def workspace(self, loop_count):
+        n = rq.decode_workspace_bytes(self.shape, loop_count, self.max_ctx)
+        return torch.empty(max(n, 16) // 4 + 4, dtype=torch.float32, device=self.device)
+
+    def decode(self, loop_begin, loop_count, out, ws, pending=True, stream=None):
+        q = self.q if loop_count == self.L else (
+            self.q_loop[loop_begin] if loop_count == 1 else
+            self.q[:, :, loop_begin:loop_begin + loop_count].contiguous())
+        pend = None
+        if pending:
+            pend = self.pending if loop_count == self.L else (
+                self.pending_loop[loop_begin] if loop_count == 1 else
+                self.pending[:, :, loop_begin:loop_begin + loop_count].contiguous())
+        rq.decode_attention(self.shape, self.cache, q, loop_begin, loop_count, pend,
+                            self.ctx_lens, self.max_ctx, out, ws, stream)
+
+    def decode_bf16(self, loop_begin, loop_count, out, ws, pending=True, stream=None):
+        q = self.q if loop_count == self.L else (
+            self.q_loop[loop_begin] if loop_count == 1 else
+            self.q[:, :, loop_begin:loop_begin + loop_count].contiguous())
+        pend = None
+        if pending:
+            pend = self.pending if loop_count == self.L else (
+                self.pending_loop[loop_begin] if loop_count == 1 else
+                self.pending[:, :, loop_begin:loop_begin + loop_count].contiguous())
+        rq.bf16_decode_attention(self.shape, self.k, self.v, q, loop_begin, loop_count, pend,
+                                 self.ctx_lens, self.max_ctx, out, ws, stream)
+
+    def out_buffer(self, loop_count):
+        return torch.empty(self.B, self.Hq, loop_count, self.d, dtype=torch.bfloat16,
+                           device=self.device)
+
+    # ------------------------------------------------------------------ readback
+    def packed_slice(self, b, h, ntok):
+        """Host copies of the packed arrays of (sequence b, kv-head h), tokens [0, ntok)."""
+        ntok += ntok % 2
+        c = self.cache
+        out = {}
+        for kv in range(2):
+            out[("ref_codes", kv)] = c.ref_codes[kv][b, h, :ntok].cpu().numpy()
+            out[("ref_meta", kv)] = c.ref_meta[kv][b, h, :ntok].float().cpu().numpy()
+            for l in range(self.L - 1):
+                out[("res_codes", kv, l)] = c.res_codes[kv][l][b, h, :ntok].cpu().numpy()
+                out[("res_meta", kv, l)] = c.res_meta[kv][l][b, h, :ntok].float().cpu().numpy()
+                out[("alpha", kv, l)] = c.alpha[kv][l][b, h, :ntok].float().cpu().numpy()
+        return out
+
+
+def np_bf16(t):
+    """bf16 torch tensor -> fp64 numpy."""
+    return t.float().cpu().numpy().astype(np.float64)

@@ -1,0 +1,190 @@
+"""GPU parity: librq (through its C ABI) against the fp64 oracle on seeded inputs."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import looped_transformer_kv_gb300 as rqm
+    from looped_transformer_kv_gb300.workload import Workload
+
+from rq_parity import check_slice, Follow, gpu_slice_to_oracle_names, packed_bytes_equal  # noqa: E402
+
+
+def _cfg(name, **kw):
+    return dataclasses.replace(synth.config_by_name(name), **kw)
+
+
+# ------------------------------------------------------------------ generator twins
+
+@pytest.mark.parametrize("name", ["pr1_small", "gqa_deep", "mixed_24l"])
+def test_gpu_generator_matches_host_generator(name):
+    cfg = synth.config_by_name(name)
+    w = Workload(cfg, capacity=64, ctx_lens=[40] * 2, batch=2, build_rq=False)
+    buf = torch.empty(2, 64, 2, cfg.n_loops, cfg.n_kv_heads, cfg.head_dim,
+                      dtype=torch.bfloat16, device="cuda")
+    rqm.synth_states(w.params, buf, buf.stride()[:5], 0, 2, 0, 64, 0, cfg.n_loops)
+    host = synth.gen_states(cfg, 0, [0, 1], np.arange(64))          # [b][t][kv][l][h][d]
+    gpu = buf.float().cpu().numpy()
+    assert np.array_equal(gpu, host)
+    qh = synth.gen_queries(cfg, 0, [0, 1])
+    assert np.array_equal(w.q.float().cpu().numpy(), qh)
+
+
+# ------------------------------------------------------------------ small shapes
+
+SMALL = [
+    # name, overrides, ctx_lens
+    ("pr1_small", {}, [256]),
+    ("layer_1p4b", dict(batch=3, n_q_heads=2, n_kv_heads=2), [257, 33, 1]),
+    ("mixed_24l", dict(batch=2, n_q_heads=2, n_kv_heads=2), [100, 0]),
+    ("gqa_deep", dict(batch=3, n_q_heads=8, n_kv_heads=2), [31, 32, 2]),
+    ("layer_1p4b", dict(batch=1, n_q_heads=4, n_kv_heads=4, n_loops=1, res_bits=()), [70]),
+    ("pr1_small", dict(n_loops=2, res_bits=(4,), sigma=(0.3, 0.1)), [300]),
+    ("pr1_small", dict(n_q_heads=8, n_kv_heads=2, n_loops=8, res_bits=(2, 4) * 3 + (2,),
+                       sigma=(0.1,) * 8), [129]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+@pytest.mark.parametrize("pending", [True, False])
+def test_small_parity(case, pending):
+    name, over, ctx = SMALL[case]
+    cfg = _cfg(name, **over)
+    cap = max(ctx) + 2
+    w = Workload(cfg, capacity=cap, ctx_lens=ctx, batch=len(ctx))
+    calls, outs = [], []
+    for l in range(cfg.n_loops):                       # causal per-loop calls
+        o = w.out_buffer(1)
+        w.decode(l, 1, o, w.workspace(1), pending=pending)
+        calls.append((l, 1))
+        outs.append(o)
+    o = w.out_buffer(cfg.n_loops)                      # all loops in one call
+    w.decode(0, cfg.n_loops, o, w.workspace(cfg.n_loops), pending=pending)
+    calls.append((0, cfg.n_loops))
+    outs.append(o)
+    if cfg.n_loops > 2:                                # a middle range
+        o2 = w.out_buffer(2)
+        w.decode(1, 2, o2, w.workspace(2), pending=pending)
+        calls.append((1, 2))
+        outs.append(o2)
+    torch.cuda.synchronize()
+    for b in range(len(ctx)):
+        for h in range(cfg.n_kv_heads):
+            check_slice(w, b, h, calls, outs, pending=pending)
+    # the multi-loop call and the per-loop calls compute the same attention
+    per = torch.cat(outs[: cfg.n_loops], dim=2).float()
+    assert torch.allclose(per, outs[cfg.n_loops].float(), atol=2e-3, rtol=1e-2)
+
+
+# ------------------------------------------------------------------ degenerate inputs
+
+def _encode_custom(x, d, L, res_bits, signs):
+    """Encode host states x [N][2][L][d] (bf16 values) through librq; returns the slice."""
+    N = x.shape[0]
+    cap = N + N % 2
+    shape = rqm.make_shape(1, 1, 1, d, L, cap, res_bits)
+    cache = rqm.PackedCache(shape, torch.from_numpy(signs[:, None, :].copy()))
+    kv = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).cuda()
+    kv = kv.reshape(1, N, 2, L, 1, d)
+    rqm.encode_append(shape, cache, kv, pos_begin=0)
+    torch.cuda.synchronize()
+    sl = {}
+    for k in range(2):
+        sl[("ref_codes", k)] = cache.ref_codes[k][0, 0, :cap].cpu().numpy()
+        sl[("ref_meta", k)] = cache.ref_meta[k][0, 0, :cap].float().cpu().numpy()
+        for l in range(L - 1):
+            sl[("res_codes", k, l)] = cache.res_codes[k][l][0, 0, :cap].cpu().numpy()
+            sl[("res_meta", k, l)] = cache.res_meta[k][l][0, 0, :cap].float().cpu().numpy()
+            sl[("alpha", k, l)] = cache.alpha[k][l][0, 0, :cap].float().cpu().numpy()
+    return sl, cap
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_degenerate_groups_encode(d):
+    rng = np.random.default_rng(0)
+    L, res_bits = 4, [2, 4, 2]
+    N = 8
+    x = O.bf16_round(rng.standard_normal((N, 2, L, d)))
+    x[0] = 0.0                                           # all zero token
+    x[1, :, :, :32] = 0.75                               # constant group in every loop
+    x[2, :, :, :] = x[2, :, L - 1:L, :]                  # all loops equal the reference
+    x[3, 1, :, 5] = 40.0                                 # outlier channel
+    x[4, :, :L - 1] = 0.0                                # zero residual loops, nonzero ref
+    x[5, :, L - 1] = 0.0                                 # zero reference: a = 0
+    signs = np.where(rng.random((2, d)) < 0.5, -1, 1).astype(np.int8)
+    sl, cap = _encode_custom(x, d, L, res_bits, signs)
+    xe = np.concatenate([x, np.zeros((cap - N, 2, L, d))]) if cap > N else x
+    for kv in range(2):
+        f = Follow(gpu_slice_to_oracle_names(sl, kv, d, L, res_bits))
+        enc = O.encode(xe[:, kv], signs[kv].astype(np.float64), res_bits, rnd=f)
+        assert f.bad == 0, f.bad_names
+        assert packed_bytes_equal(enc, sl, kv, res_bits)
+    assert np.all(sl[("alpha", 0, 0)][5] == 0.0)
+
+
+def test_on_grid_reference_gives_zero_residual_on_gpu():
+    rng = np.random.default_rng(4)
+    d, L, N = 128, 4, 6
+    codes = rng.integers(0, 16, size=(N, d // 32, 32))
+    codes[:, :, 0], codes[:, :, 1] = 0, 15
+    s = 2.0 ** rng.integers(-5, 0, size=(N, d // 32, 1))
+    ref = (codes * s + rng.integers(-8, 2, size=(N, d // 32, 1)) * s).reshape(N, d)
+    x = np.repeat(np.repeat(ref[:, None, None, :], 2, axis=1), L, axis=2)
+    signs = np.where(rng.random((2, d)) < 0.5, -1, 1).astype(np.int8)
+    sl, _ = _encode_custom(x, d, L, [2, 2, 2], signs)
+    for kv in range(2):
+        for l in range(L - 1):
+            assert np.all(sl[("alpha", kv, l)][:N] == 1.0)
+            assert np.all(sl[("res_codes", kv, l)][:N] == 0)
+            assert np.all(sl[("res_meta", kv, l)][:N] == 0.0)
+
+
+# ------------------------------------------------------------------ BF16 comparison kernel
+
+@pytest.mark.parametrize("name,over,ctx", [
+    ("pr1_small", {}, [256]),
+    ("gqa_deep", dict(batch=2, n_q_heads=8, n_kv_heads=2), [300, 5]),
+])
+def test_bf16_kernel_matches_textbook_attention(name, over, ctx):
+    cfg = _cfg(name, **over)
+    w = Workload(cfg, capacity=max(ctx) + 2, ctx_lens=ctx, batch=len(ctx), build_rq=False,
+                 build_bf16=True)
+    o = w.out_buffer(cfg.n_loops)
+    w.decode_bf16(0, cfg.n_loops, o, w.workspace(cfg.n_loops))
+    torch.cuda.synchronize()
+    got = o.float().cpu().numpy()
+    g = cfg.n_q_heads // cfg.n_kv_heads
+    for b, c in enumerate(ctx):
+        x = synth.gen_states(cfg, 0, [b], np.arange(c + 1))[0].astype(np.float64)  # [t][kv][l][h][d]
+        q = synth.gen_queries(cfg, 0, [b])[0].astype(np.float64)
+        for hq in range(cfg.n_q_heads):
+            h = hq // g
+            for l in range(cfg.n_loops):
+                ref = O.softmax_attention(q[hq, l][None], x[:, 0, l, h], x[:, 1, l, h],
+                                          1 / np.sqrt(cfg.head_dim))[0]
+                e = np.abs(got[b, hq, l] - ref)
+                from rq_parity import bf16_half_ulp
+                assert np.max(e - bf16_half_ulp(ref)) <= 2e-3
+
+
+# ------------------------------------------------------------------ status codes
+
+def test_invalid_calls_return_status_and_enqueue_nothing():
+    cfg = _cfg("pr1_small")
+    w = Workload(cfg, capacity=64, ctx_lens=[10], batch=1)
+    o = w.out_buffer(1)
+    small = torch.empty(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(rqm.rq._lib.RqError) as e:
+        w.decode(0, 1, o, small)
+    assert e.value.status == 3
+    with pytest.raises(rqm.rq._lib.RqError) as e:
+        w.decode(3, 2, o, w.workspace(2))
+    assert e.value.status == 1
