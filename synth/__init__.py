@@ -16,6 +16,8 @@ from .recipe import (  # noqa: F401
     CONFIGS,
     config_by_name,
     outlier_channels,
+    outlier_table,
+    round_bf16_f32,
     rotation_signs,
     gen_states,
     gen_queries,
