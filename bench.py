@@ -210,19 +210,35 @@ def gpu_arm(args, cfg):
     g = w.Hq // w.H
     launches_per_step = math.ceil(g * L / 8) + 1 + 1
 
-    def timeit(fn, iters):
+    def graph_of(fn):
+        """Capture fn (a sequence of library calls on the current stream) in a CUDA graph."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        torch.cuda.synchronize()
+        return gr
+
+    def timeit(gr, iters):
+        """Per-replay device times (ms) of a captured graph, CUDA events on this stream."""
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
         torch.cuda.synchronize()
         ev[0].record(stream)
         for i in range(iters):
-            fn()
+            gr.replay()
             ev[i + 1].record(stream)
         torch.cuda.synchronize()
         return [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
 
+    g_step = graph_of(step)
     # ---- warm-up, then the timed steps (barrier + synchronize on both sides) ----
     for _ in range(args.warmup):
-        step()
+        g_step.replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -232,7 +248,7 @@ def gpu_arm(args, cfg):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for _ in range(args.steps):
-        step()
+        g_step.replay()
     stop.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / args.steps
@@ -242,25 +258,26 @@ def gpu_arm(args, cfg):
         ms = float(t.item())
         dist.barrier()
 
-    # ---- per-kernel timings (same stream, CUDA events) ----
+    # ---- per-call timings (graph replays, same stream, CUDA events) ----
     iters = max(args.steps, 20)
-    t_dec = timeit(lambda: w.decode(0, L, out, ws), iters)
-    t_enc = timeit(lambda: rqm.encode_append(w.shape, w.cache, new_kv, positions=pos_new), iters)
+    t_dec = timeit(graph_of(lambda: w.decode(0, L, out, ws)), iters)
+    t_enc = timeit(graph_of(lambda: rqm.encode_append(w.shape, w.cache, new_kv, positions=pos_new)),
+                   iters)
 
     def perloop():
         for l in range(L):
             w.decode(l, 1, out1[l], ws1)
 
-    t_per = timeit(perloop, iters)
+    t_per = timeit(graph_of(perloop), iters)
     t_bf_multi = t_bf_per = None
     if not args.no_bf16:
-        t_bf_multi = timeit(lambda: w.decode_bf16(0, L, out, ws), iters)
+        t_bf_multi = timeit(graph_of(lambda: w.decode_bf16(0, L, out, ws)), iters)
 
         def bf_per():
             for l in range(L):
                 w.decode_bf16(l, 1, out1[l], ws1)
 
-        t_bf_per = timeit(bf_per, iters)
+        t_bf_per = timeit(graph_of(bf_per), iters)
     clk = clocks.stop()
 
     # ---- end to end through the public API with host buffers ----
@@ -276,7 +293,14 @@ def gpu_arm(args, cfg):
 
     for _ in range(2):
         e2e_step()
-    t_e2e = statistics.mean(timeit(e2e_step, args.steps))
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = ev0.elapsed_time(ev1) / args.steps
     h2d = q_h.numel() * 2 + p_h.numel() * 2
     d2h = o_h.numel() * 2
 
@@ -323,7 +347,8 @@ def gpu_arm(args, cfg):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded Philox generator; no dataset)",
         "config": {"workload": _workload_desc(cfg), "step": "multi-loop decode attention + "
-                   "deferred-write encode/append of the current token", "layers_timed": 1,
+                   "deferred-write encode/append of the current token (CUDA graph replay)",
+                   "layers_timed": 1,
                    "l2": "inputs larger than L2 (%.0f MB packed cache read per step)" %
                    (bytes_multi / 1e6), "parallelism": "replicas (weak, per-GPU batch %d)" % B},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",

@@ -36,8 +36,9 @@
  * A token's code row packs channel i into byte i*b/8 at bit offset (i*b) % 8.  K rows
  * are stored one after another.  V rows are stored in token pairs: for tokens 2p and
  * 2p+1 the 16-bit units of the two rows alternate (unit u of token 2p, unit u of token
- * 2p+1, unit u+1 of token 2p, ...), so capacity must be even.  Groups are 32 contiguous
- * channels: original channels for the reference, rotated channels for residuals.
+ * 2p+1, unit u+1 of token 2p, ...).  Capacity must be a multiple of 64 (the decode kernel
+ * moves whole 64-token tiles).  Groups are 32 contiguous channels: original channels for the
+ * reference, rotated channels for residuals.
  */
 #ifndef RQ_H_
 #define RQ_H_
@@ -67,7 +68,7 @@ typedef struct {
   int32_t head_dim;     /* d: 64 or 128                                               */
   int32_t n_loops;      /* L: 1..16; loop L-1 is the reference                         */
   int32_t group;        /* must be 32                                                  */
-  int32_t capacity;     /* tokens per (sequence, kv-head) slot in the cache; even      */
+  int32_t capacity;     /* tokens per (sequence, kv-head) slot; a multiple of 64       */
   int8_t res_bits[RQ_MAX_LOOPS]; /* residual bits of loop l < L-1: 2 or 4              */
   float softmax_scale;  /* 0 => 1/sqrt(d)                                              */
 } rq_shape;
@@ -105,7 +106,9 @@ rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache,
                            void* stream);
 
 /* Workspace bytes needed by rq_decode_attention / rq_bf16_decode_attention for this
- * shape, loop_count and max_ctx on the current device (split-KV partials). */
+ * shape, loop_count and max_ctx on the current device: a 256-byte header followed by the
+ * split-KV partials.  After rq_decode_attention completes, the header's first uint32 is 0;
+ * it is nonzero if a pipeline wait inside the kernel gave up (outputs are then NaN). */
 size_t rq_decode_workspace_bytes(const rq_shape* shape, int32_t loop_count, int32_t max_ctx);
 
 /* Fused decode attention over the packed cache (rit.work summary, "How each pass's KV
@@ -122,7 +125,8 @@ size_t rq_decode_workspace_bytes(const rq_shape* shape, int32_t loop_count, int3
  *   max_ctx    host upper bound of ctx_lens (<= capacity); sizes the split-KV grid.
  *   out        bf16 [B][Hq][loop_count][d].  A row with no cached and no pending token
  *              is written as zeros.
- *   ws         device workspace of at least rq_decode_workspace_bytes(...) bytes.
+ *   ws         device workspace of at least rq_decode_workspace_bytes(...) bytes,
+ *              256-byte aligned.
  * Loop-l queries attend over loop l's rebuilt K/V; scores are scaled by softmax_scale. */
 rq_status rq_decode_attention(const rq_shape* shape, const rq_cache* cache,
                               const uint16_t* q, int32_t loop_begin, int32_t loop_count,
@@ -132,7 +136,7 @@ rq_status rq_decode_attention(const rq_shape* shape, const rq_cache* cache,
 
 /* Comparison kernel: the same decode attention over an uncompressed BF16 cache,
  *   k, v  bf16 [B][Hkv][L][capacity][d]
- * with every other argument as in rq_decode_attention. */
+ * with every other argument as in rq_decode_attention (Hq / Hkv at most 8). */
 rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k,
                                    const uint16_t* v, const uint16_t* q, int32_t loop_begin,
                                    int32_t loop_count, const uint16_t* pending_kv,

@@ -14,7 +14,7 @@ rq_status check_shape(const rq_shape* s) {
       s->n_loops <= 0)
     return RQ_ERR_INVALID_ARG;
   if (s->n_q_heads % s->n_kv_heads != 0) return RQ_ERR_INVALID_ARG;
-  if (s->capacity % 2 != 0) return RQ_ERR_INVALID_ARG;
+  if (s->capacity % 64 != 0) return RQ_ERR_INVALID_ARG;
   if (s->group != 32) return RQ_ERR_UNSUPPORTED;
   if (s->head_dim != 64 && s->head_dim != 128) return RQ_ERR_UNSUPPORTED;
   if (s->n_loops > RQ_MAX_LOOPS) return RQ_ERR_UNSUPPORTED;
@@ -47,7 +47,7 @@ rq_status check_decode(const rq_shape* s, const uint16_t* q, int32_t loop_begin,
     return RQ_ERR_UNSUPPORTED;
   const size_t need = rq_decode_workspace_bytes(s, loop_count, max_ctx);
   if (!ws || ws_bytes < need) return RQ_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(ws) & 15) != 0) return RQ_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return RQ_ERR_WORKSPACE;
   return RQ_OK;
 }
 
@@ -88,8 +88,9 @@ rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache, const u
 size_t rq_decode_workspace_bytes(const rq_shape* s, int32_t loop_count, int32_t max_ctx) {
   if (check_shape(s) != RQ_OK || loop_count < 1 || max_ctx < 0) return 0;
   const rq::SplitPlan p = rq::plan_splits(*s, loop_count, max_ctx);
-  return size_t(s->batch) * s->n_q_heads * loop_count * p.n_splits * rq::partial_floats(*s) *
-         sizeof(float);
+  return size_t(rq::kWsHeaderBytes) +
+         size_t(s->batch) * s->n_q_heads * loop_count * p.n_splits * rq::partial_floats(*s) *
+             sizeof(float);
 }
 
 rq_status rq_decode_attention(const rq_shape* shape, const rq_cache* cache, const uint16_t* q,

@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kWarps * 32) bf16_split_kernel(Bf16Args a) {
     for (int j = 0; j < P; ++j) acc_sm[warp][n][lane * P + j] = acc[n][j];
   }
   __syncthreads();
-  const int rec = 2 + 2 * D;
+  const int rec = int(partial_floats_d(D));
   for (int n = warp; n < a.g; n += kWarps) {
     float M = -INFINITY;
 #pragma unroll
@@ -164,8 +164,8 @@ __global__ void __launch_bounds__(kWarps * 32) bf16_split_kernel(Bf16Args a) {
       float v = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) v += f[w] * acc_sm[w][n][i];
-      out[2 + i] = v;
-      out[2 + D + i] = 0.f;
+      out[4 + i] = v;
+      out[4 + D + i] = 0.f;
     }
   }
 }
@@ -185,6 +185,7 @@ cudaError_t launch_bf16_decode(const rq_shape& s, const uint16_t* k, const uint1
                                const uint16_t* pending, const int32_t* ctx_lens, int max_ctx,
                                uint16_t* out, float* ws, cudaStream_t stream) {
   const SplitPlan plan = plan_splits(s, loop_count, max_ctx);
+  ws += kWsHeaderBytes / sizeof(float);
   Bf16Args a;
   a.k = k;
   a.v = v;
@@ -210,7 +211,8 @@ cudaError_t launch_bf16_decode(const rq_shape& s, const uint16_t* k, const uint1
     launch_d<64>(a, grid, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_combine(s, nullptr, q, loop_count, pending, plan.n_splits, out, ws, stream);
+  return launch_combine(s, nullptr, q, loop_count, pending, plan.n_splits, out, ws, nullptr,
+                        stream);
 }
 
 }  // namespace rq

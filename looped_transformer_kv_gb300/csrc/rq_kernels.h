@@ -8,6 +8,50 @@
 
 namespace rq {
 
+constexpr int kMaxResPerBlock = 8;   // residual loops handled by one decode launch
+constexpr int kWsHeaderBytes = 256;  // workspace header: uint32 error word, then padding
+
+// A block of query columns handled by one launch: query heads [gi0, gi0 + gw) of each
+// kv-head (gw a power of two <= 8) for loops [lb, lb + nl); residual loops [r0, r0 + nr).
+struct QueryBlock {
+  int gi0, gw, lb, nl, r0, nr;
+};
+
+// Shared-memory layout of the tensor-core decode kernel (byte offsets).
+struct SmemLayout {
+  int qf, qrf, qsum, qrs, ps, pa, red, mrun, bars, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int D, int NT, int nr, int stages,
+                                                  int stage_bytes) {
+  const int NG = D / 32, NQP = NT * 8;
+  SmemLayout s;
+  int o = stages * stage_bytes;
+  o = (o + 15) & ~15;
+  s.qf = o;   o += NG * 2 * NT * 32 * 8;
+  s.qrf = o;  o += nr * NG * 2 * 32 * 8;
+  s.qsum = o; o += NG * NQP * 4;
+  s.qrs = o;  o += nr * NG * 8 * 4;
+  s.ps = o;   o += 64 * NQP * 4;
+  s.pa = o;   o += 64 * NQP * 4;
+  s.red = o;  o += 4 * NQP * 4;
+  s.mrun = o; o += NQP * 4;
+  o = (o + 7) & ~7;
+  s.bars = o; o += stages * 8;
+  s.total = o;
+  return s;
+}
+
+// Split partial record: m, l, two pad floats, acc_ref[D], acc_res[D] (16-byte aligned rows).
+__host__ __device__ constexpr size_t partial_floats_d(int D) { return size_t(4 + 2 * D); }
+
+int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* out, int max_out);
+
+cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const uint16_t* q,
+                                 int loop_begin, int loop_count, const int32_t* ctx_lens,
+                                 int n_splits, int tokens_per_split, float* part, unsigned* err,
+                                 cudaStream_t stream);
+
 struct SplitPlan {
   int n_splits;          // split-KV partitions of the context
   int tokens_per_split;  // multiple of the kernel's token chunk
@@ -32,7 +76,8 @@ cudaError_t launch_bf16_decode(const rq_shape& s, const uint16_t* k, const uint1
 
 cudaError_t launch_combine(const rq_shape& s, const int8_t* v_signs, const uint16_t* q,
                            int loop_count, const uint16_t* pending, int n_splits,
-                           uint16_t* out, const float* ws, cudaStream_t stream);
+                           uint16_t* out, const float* part, const unsigned* err,
+                           cudaStream_t stream);
 
 int device_sm_count();
 

@@ -23,7 +23,7 @@ class Workload:
         B = cfg.batch if batch is None else batch
         H, Hq, d, L = cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim, cfg.n_loops
         cap = cfg.ctx if capacity is None else capacity
-        cap += cap % 2
+        cap = max(64, -(-cap // 64) * 64)                # whole 64-token tiles
         self.B, self.H, self.Hq, self.d, self.L, self.cap = B, H, Hq, d, L, cap
         if ctx_lens is None:
             ctx_lens = [min(cfg.ctx, cap)] * B
