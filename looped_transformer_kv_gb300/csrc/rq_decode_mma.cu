@@ -14,7 +14,9 @@
 // the code bits, masked in place, sit in the low mantissa bits of 1024 (0x6400), and
 // subtracting 1024 leaves the code times a power of two fixed by its bit position; that
 // power is folded into the query fragments (scores) or removed per output row at the end
-// (values).  Products of fp16 operands are exact in the fp32 accumulators.
+// (values).  Products of fp16 operands are exact in the fp32 accumulators.  The other
+// operand (queries, softmax weights) is split into an fp16 high part and an fp16 low part
+// (two MMAs), so it carries about 22 significant bits.
 // Per-(token, group) steps and offsets are applied in fp32 to the score fragments and
 // folded into P for the values; the offsets' value terms are accumulated separately.
 #include <mutex>
@@ -87,8 +89,8 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
   const int nr = blk.nr;
 
   const SmemLayout lay = smem_layout(D, NT, nr, a.n_stages, a.stage_bytes);
-  uint2* QF = reinterpret_cast<uint2*>(smem + lay.qf);
-  uint2* QRF = reinterpret_cast<uint2*>(smem + lay.qrf);
+  uint4* QF = reinterpret_cast<uint4*>(smem + lay.qf);    // {b0, b1} high parts, {b0, b1} low
+  uint4* QRF = reinterpret_cast<uint4*>(smem + lay.qrf);
   float* Qsum = reinterpret_cast<float*>(smem + lay.qsum);
   float* QRS = reinterpret_cast<float*>(smem + lay.qrs);
   float* Ps = reinterpret_cast<float*>(smem + lay.ps);
@@ -151,20 +153,20 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
       {  // 4-bit mapping: slot (c4, s, hi, e) <- channel 8 c4 + 2 s + hi + 4 e, scale 16^-hi
         const int c4 = cl >> 3, w8 = cl & 7, s = (w8 >> 1) & 1, hi = w8 & 1, e = w8 >> 2;
         __half* dst = reinterpret_cast<__half*>(&QF[((gq * 2 + s) * NT + nt) * 32 + nn * 4 + c4]);
-        dst[hi * 2 + e] = __float2half_rn(hi ? v[j] * 0.0625f : v[j]);
+        split_half(hi ? v[j] * 0.0625f : v[j], dst[hi * 2 + e], dst[4 + hi * 2 + e]);
       }
       if (ri >= 0) {
         __half* base = reinterpret_cast<__half*>(QRF);
         if (a.rbits[ri] == 4) {
           const int c4 = cl >> 3, w8 = cl & 7, s = (w8 >> 1) & 1, hi = w8 & 1, e = w8 >> 2;
-          base[(((ri * NG + gq) * 2 + s) * 32 + nn * 4 + c4) * 4 + hi * 2 + e] =
-              __float2half_rn(hi ? rr[j] * 0.0625f : rr[j]);
+          __half* dst = base + (((ri * NG + gq) * 2 + s) * 32 + nn * 4 + c4) * 8;
+          split_half(hi ? rr[j] * 0.0625f : rr[j], dst[hi * 2 + e], dst[4 + hi * 2 + e]);
         } else {  // 2-bit mapping: slot (cq, s, hi, e) <- channel 16(cq/2) + 4(cq%2) + 2s + hi + 8e
           const int e = (cl >> 3) & 1, cq = 2 * (cl >> 4) + ((cl & 7) >> 2), jj = cl & 3;
           const int s = jj >> 1, hi = jj & 1;
           const float sc = (jj == 0) ? 1.f : (jj == 1) ? 0.25f : (jj == 2) ? 0.0625f : 0.015625f;
-          base[(((ri * NG + gq) * 2 + s) * 32 + nn * 4 + cq) * 4 + hi * 2 + e] =
-              __float2half_rn(rr[j] * sc);
+          __half* dst = base + (((ri * NG + gq) * 2 + s) * 32 + nn * 4 + cq) * 8;
+          split_half(rr[j] * sc, dst[hi * 2 + e], dst[4 + hi * 2 + e]);
         }
       }
     }
@@ -262,8 +264,9 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
           const uint32_t a2 = code_pair(xl, 0x00F000F0u), a3 = code_pair(xh, 0x00F000F0u);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 bq = QF[((gq * 2 + s) * NT + nt) * 32 + lane];
+            const uint4 bq = QF[((gq * 2 + s) * NT + nt) * 32 + lane];
             mma_f16(Dg[nt], a0, a1, a2, a3, bq.x, bq.y);
+            mma_f16(Dg[nt], a0, a1, a2, a3, bq.z, bq.w);
           }
         }
         const float s0 = m0.x * kCodeUnit, s1 = m1.x * kCodeUnit;
@@ -310,8 +313,9 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
               a2 = code_pair(xl, 0x00F000F0u);
               a3 = code_pair(xh, 0x00F000F0u);
             }
-            const uint2 bq = QRF[((ri * NG + gq) * 2 + s) * 32 + lane];
+            const uint4 bq = QRF[((ri * NG + gq) * 2 + s) * 32 + lane];
             mma_f16(Dg, a0, a1, a2, a3, bq.x, bq.y);
+            mma_f16(Dg, a0, a1, a2, a3, bq.z, bq.w);
           }
           const float2 qs = *reinterpret_cast<const float2*>(&QRS[(ri * NG + gq) * 8 + 2 * c]);
           const float s0 = m0.x * kCodeUnit, s1 = m1.x * kCodeUnit;
@@ -374,6 +378,18 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
       mnew_mine = fmaxf(mrun[threadIdx.x], mt);
     }
     const bool v0 = t0 + tr0 < t_end, v1 = t0 + tr1 < t_end;
+    // rescale of the value-offset sums, kept per B-fragment column nt*8 + r
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = nt * 8 + r;
+      float mt = red[col];
+#pragma unroll
+      for (int w = 1; w < kW; ++w) mt = fmaxf(mt, red[w * NQP + col]);
+      const float mo = mrun[col];
+      const float cb = (mo == -INFINITY) ? 0.f : exp2f(mo - fmaxf(mo, mt));
+      offR[nt] *= cb;
+      offE[nt] *= cb;
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -437,7 +453,7 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
           vs[k] = mm.x;
           vz[k] = mm.y;
         }
-        uint32_t bR[NT][2];
+        uint32_t bR[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int n = nt * 8 + r;
@@ -448,8 +464,8 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
             w[k] = val[k] ? pa * vs[k] : 0.f;
             offR[nt] += val[k] ? pa * vz[k] : 0.f;
           }
-          bR[nt][0] = pack_half2(w[0], w[1]);
-          bR[nt][1] = pack_half2(w[2], w[3]);
+          split_half2(w[0], w[1], bR[nt][0], bR[nt][2]);
+          split_half2(w[2], w[3], bR[nt][1], bR[nt][3]);
         }
         const uint32_t W0 = lds32(sb + a.off_vc + p0 * D + (8 * gv + r) * 4);
         const uint32_t W1 = lds32(sb + a.off_vc + p1 * D + (8 * gv + r) * 4);
@@ -460,7 +476,10 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
           const uint32_t a0 = code_pair(x0, 0x000F000Fu), a1 = code_pair(x0, 0x00F000F0u);
           const uint32_t a2 = code_pair(x1, 0x000F000Fu), a3 = code_pair(x1, 0x00F000F0u);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16(accR[m][nt], a0, a1, a2, a3, bR[nt][0], bR[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_f16(accR[m][nt], a0, a1, a2, a3, bR[nt][0], bR[nt][1]);
+            mma_f16(accR[m][nt], a0, a1, a2, a3, bR[nt][2], bR[nt][3]);
+          }
         }
       }
       // residual values of each loop in the block
@@ -482,7 +501,9 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
           for (int nt = 0; nt < NT; ++nt)
             if (nt == nt_ri) offE[nt] += oz;
         }
-        const uint32_t b0 = pack_half2(w[0], w[1]), b1 = pack_half2(w[2], w[3]);
+        uint32_t b0, b1, b0l, b1l;
+        split_half2(w[0], w[1], b0, b0l);
+        split_half2(w[2], w[3], b1, b1l);
         if (a.rbits[ri] == 2) {
           const int sh = 8 * (r & 1);
           const uint32_t W0 = lds32(sb + a.off_vrc[ri] + p0 * (2 * RB2) + (4 * gv + (r >> 1)) * 4) >> sh;
@@ -495,7 +516,10 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
             const uint32_t a2 = code_pair(W1, mlo), a3 = code_pair(W1, mhi);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-              if (nt == nt_ri) mma_f16(accE2[m][nt], a0, a1, a2, a3, b0, b1);
+              if (nt == nt_ri) {
+                mma_f16(accE2[m][nt], a0, a1, a2, a3, b0, b1);
+                mma_f16(accE2[m][nt], a0, a1, a2, a3, b0l, b1l);
+              }
           }
         } else if (RES4) {
           const uint32_t W0 = lds32(sb + a.off_vrc[ri] + p0 * D + (8 * gv + r) * 4);
@@ -508,7 +532,10 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
             const uint32_t a2 = code_pair(x1, 0x000F000Fu), a3 = code_pair(x1, 0x00F000F0u);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-              if (nt == nt_ri) mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, b0, b1);
+              if (nt == nt_ri) {
+                mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, b0, b1);
+                mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, b0l, b1l);
+              }
           }
         }
       }

@@ -28,8 +28,8 @@ __host__ __device__ inline SmemLayout smem_layout(int D, int NT, int nr, int sta
   SmemLayout s;
   int o = stages * stage_bytes;
   o = (o + 15) & ~15;
-  s.qf = o;   o += NG * 2 * NT * 32 * 8;
-  s.qrf = o;  o += nr * NG * 2 * 32 * 8;
+  s.qf = o;   o += NG * 2 * NT * 32 * 16;   // hi and lo f16x2 pairs per lane
+  s.qrf = o;  o += nr * NG * 2 * 32 * 16;
   s.qsum = o; o += NG * NQP * 4;
   s.qrs = o;  o += nr * NG * 8 * 4;
   s.ps = o;   o += 64 * NQP * 4;
