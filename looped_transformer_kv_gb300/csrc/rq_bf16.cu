@@ -184,7 +184,7 @@ cudaError_t launch_bf16_decode(const rq_shape& s, const uint16_t* k, const uint1
                                const uint16_t* q, int loop_begin, int loop_count,
                                const uint16_t* pending, const int32_t* ctx_lens, int max_ctx,
                                uint16_t* out, float* ws, cudaStream_t stream) {
-  const SplitPlan plan = plan_splits(s, loop_count, max_ctx);
+  const SplitPlan plan = plan_splits_bf16(s, max_ctx);
   ws += kWsHeaderBytes / sizeof(float);
   Bf16Args a;
   a.k = k;

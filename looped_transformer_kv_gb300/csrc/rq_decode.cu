@@ -104,22 +104,40 @@ int device_sm_count() {
   return n;
 }
 
-SplitPlan plan_splits(const rq_shape& s, int loop_count, int max_ctx) {
-  (void)loop_count;
+SplitPlan plan_splits_for(const rq_shape& s, int max_ctx, int ctas_per_sm, int chunk) {
   SplitPlan p;
-  const int units = s.batch * s.n_kv_heads;
-  const int target = device_sm_count() * 4;
-  int max_splits = (max_ctx + kSplitChunk - 1) / kSplitChunk;
-  if (max_splits < 1) max_splits = 1;
-  int splits = (target + units - 1) / units;
-  splits = splits < 1 ? 1 : (splits > max_splits ? max_splits : splits);
-  if (splits > 256) splits = 256;
-  int per = (max_ctx + splits - 1) / splits;
-  per = ((per + kSplitChunk - 1) / kSplitChunk) * kSplitChunk;
-  if (per < kSplitChunk) per = kSplitChunk;
-  p.tokens_per_split = per;
-  p.n_splits = max_ctx > 0 ? (max_ctx + per - 1) / per : 1;
+  const int64_t units = int64_t(s.batch) * s.n_kv_heads;
+  const int64_t slots = int64_t(device_sm_count()) * (ctas_per_sm < 1 ? 1 : ctas_per_sm);
+  const int tiles = max_ctx > 0 ? (max_ctx + chunk - 1) / chunk : 1;
+  double best = 1e300;
+  int best_per = tiles;
+  for (int splits = 1; splits <= tiles && splits <= 256; ++splits) {
+    const int per = (tiles + splits - 1) / splits;           // tiles per split
+    const int real = (tiles + per - 1) / per;
+    const int64_t waves = (units * real + slots - 1) / slots;
+    const double cost = double(waves) * (per + 1.0);         // + one tile of set-up per split
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_per = per;
+    }
+  }
+  p.tokens_per_split = best_per * chunk;
+  p.n_splits = (tiles + best_per - 1) / best_per;
   return p;
+}
+
+SplitPlan plan_splits_bf16(const rq_shape& s, int max_ctx) {
+  return plan_splits_for(s, max_ctx, 8, kSplitChunk);
+}
+
+SplitPlan plan_splits(const rq_shape& s, int loop_count, int max_ctx) {
+  // the larger of the two kernels' plans over every loop range of this length
+  SplitPlan best = plan_splits_bf16(s, max_ctx);
+  for (int lb = 0; lb + loop_count <= s.n_loops; ++lb) {
+    const SplitPlan p = plan_splits_rq(s, lb, loop_count, max_ctx);
+    if (p.n_splits > best.n_splits) best = p;
+  }
+  return best;
 }
 
 size_t partial_floats(const rq_shape& s) { return partial_floats_d(s.head_dim); }
@@ -128,7 +146,7 @@ cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const uin
                              int loop_begin, int loop_count, const uint16_t* pending,
                              const int32_t* ctx_lens, int max_ctx, uint16_t* out, float* ws,
                              cudaStream_t stream) {
-  const SplitPlan plan = plan_splits(s, loop_count, max_ctx);
+  const SplitPlan plan = plan_splits_rq(s, loop_begin, loop_count, max_ctx);
   unsigned* err = reinterpret_cast<unsigned*>(ws);
   float* part = ws + kWsHeaderBytes / sizeof(float);
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream);

@@ -4,21 +4,23 @@
 // packed array are staged in shared memory by 1-D bulk (TMA) copies through a multi-stage
 // mbarrier pipeline.  For a loop-l query q and token t (rit.work summary, "How each pass's
 // KV cache is reconstructed": reference and residuals rebuilt inside attention)
-//   score_t = a_t * sum_g s^r_g,t (q_g . c^r_g,t) + z^r_g,t sum(q_g)
-//           +       sum_g s^e_g,t (q'_g . c^e_g,t) + z^e_g,t sum(q'_g),     q' = R q
-//   acc_ref += p_t a_t (s^r c^r + z^r),  acc_res += p_t (s^e c^e + z^e)   (rotated domain)
+//   score_t = a_t * sum_g [s^r_g,t (q_g . c^r_g,t) + z^r_g,t sum(q_g)]
+//           +       sum_g [s^e_g,t (q'_g . c^e_g,t) + z^e_g,t sum(q'_g)],      q' = R q
+//   acc_ref += p_t a_t (s^r c^r + z^r),   acc_res += p_t (s^e c^e + z^e)   (rotated domain)
 // The code dot products and the P.V products run as mma.sync m16n8k16 (f16 in, f32 acc):
-//   scores: M = 16 tokens, N = 8 queries, K = 16 channels of one 32-channel group;
-//   values: M = 16 channels of one group, N = 8 queries, K = 16 tokens.
+//   scores: M = 16 tokens, N = 8 query columns, K = 16 channels of one 32-channel group;
+//   values: M = 16 channels of one group, N = 8 query columns, K = 16 tokens.
 // A pair of packed codes becomes an f16x2 operand with one LOP3 and one packed subtract:
 // the code bits, masked in place, sit in the low mantissa bits of 1024 (0x6400), and
 // subtracting 1024 leaves the code times a power of two fixed by its bit position; that
 // power is folded into the query fragments (scores) or removed per output row at the end
-// (values).  Products of fp16 operands are exact in the fp32 accumulators.  The other
-// operand (queries, softmax weights) is split into an fp16 high part and an fp16 low part
-// (two MMAs), so it carries about 22 significant bits.
-// Per-(token, group) steps and offsets are applied in fp32 to the score fragments and
-// folded into P for the values; the offsets' value terms are accumulated separately.
+// (values).  The other operand (queries, softmax weights) is split into an fp16 high part
+// and an fp16 low part (two MMAs) and so carries about 22 significant bits; products are
+// exact in the fp32 accumulators.
+// Query columns of every loop share the fragments: the residual codes of loop l meet a
+// query fragment whose columns of other loops are masked to zero, so all residual loops
+// accumulate into one score fragment per group (scaled once by each column's own step and
+// offset) and into one value accumulator per residual bit width.
 #include <mutex>
 
 #include "rq_common.cuh"
@@ -31,7 +33,6 @@ namespace {
 constexpr int kT = 64;                        // tokens per tile
 constexpr int kW = 4;                         // warps per CTA
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr float kCodeUnit = 1.0f;    // fp16 code operands hold the code values exactly
 
 struct MmaArgs {
   const uint8_t* kc;
@@ -64,12 +65,40 @@ __device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
 }
 
 __device__ __forceinline__ float2 ld_meta(const uint8_t* p) {  // (step, offset) fp16 pair
-  const __half2 h = *reinterpret_cast<const __half2*>(p);
-  return __half22float2(h);
+  return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
 
 __device__ __forceinline__ float ld_half(const uint8_t* p) {
   return __half2float(*reinterpret_cast<const __half*>(p));
+}
+
+// arr[i] for a runtime i < kMaxResPerBlock without indexing the parameter array at run time
+__device__ __forceinline__ int pick_int(const int (&arr)[kMaxResPerBlock], int i) {
+  int v = arr[0];
+#pragma unroll
+  for (int k = 1; k < kMaxResPerBlock; ++k) v = (i == k) ? arr[k] : v;
+  return v;
+}
+
+__device__ __forceinline__ uint4 sel4(bool keep, uint4 v) {
+  return keep ? v : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// 4-bit group row (16 bytes) of one token: the A-operand pairs of k-step s for this lane's
+// word; slot order (2c, 2c+1 | 2c+8, 2c+9) <- channels (8c+2s, 8c+2s+4 | 8c+2s+1, 8c+2s+5),
+// the second pair scaled by 16.
+__device__ __forceinline__ void a_pairs_4bit(uint32_t w, int s, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = s ? (w >> 8) : w;
+  lo = code_pair(x, 0x000F000Fu);
+  hi = code_pair(x, 0x00F000F0u);
+}
+
+// 2-bit group row (8 bytes): this lane's byte-half of word c/2; k-step s uses codes 2s and
+// 2s+1 of each half (channels 16(c/2) + 4(c%2) + 2s + {0, 1} and +8), scaled by 4^(2s) and
+// 4^(2s+1).
+__device__ __forceinline__ void a_pairs_2bit(uint32_t x, int s, uint32_t& lo, uint32_t& hi) {
+  lo = code_pair(x, 0x00030003u << (4 * s));
+  hi = code_pair(x, 0x00030003u << (4 * s + 2));
 }
 
 template <int D, int NT, bool RES4>
@@ -88,21 +117,31 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
   const QueryBlock blk = a.blk;
   const int nr = blk.nr;
 
-  const SmemLayout lay = smem_layout(D, NT, nr, a.n_stages, a.stage_bytes);
-  uint4* QF = reinterpret_cast<uint4*>(smem + lay.qf);    // {b0, b1} high parts, {b0, b1} low
-  uint4* QRF = reinterpret_cast<uint4*>(smem + lay.qrf);
+  const SmemLayout lay = smem_layout(D, NT, RES4, a.n_stages, a.stage_bytes);
+  const int PR = lay.prow;
+  uint4* QF = reinterpret_cast<uint4*>(smem + lay.qf);
+  uint4* QR2 = reinterpret_cast<uint4*>(smem + lay.qr2);
+  uint4* QR4 = reinterpret_cast<uint4*>(smem + lay.qr4);
   float* Qsum = reinterpret_cast<float*>(smem + lay.qsum);
-  float* QRS = reinterpret_cast<float*>(smem + lay.qrs);
+  float* QRsum = reinterpret_cast<float*>(smem + lay.qrsum);
   float* Ps = reinterpret_cast<float*>(smem + lay.ps);
   float* Pa = reinterpret_cast<float*>(smem + lay.pa);
   float* red = reinterpret_cast<float*>(smem + lay.red);
   float* mrun = reinterpret_cast<float*>(smem + lay.mrun);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
 
+  // residual index (into the block's residual loops) of query column n, -1 if the column
+  // is the final loop's or a padding column
+  auto col_ri = [&](int n) -> int {
+    const int li = n / blk.gw, gi = blk.gi0 + n % blk.gw;
+    const int l = blk.lb + li;
+    return (li < blk.nl && gi < a.g && l != a.L - 1) ? l - blk.r0 : -1;
+  };
+
   // ------------------------------------------------------------------ query preparation
   {
     uint32_t* z32 = reinterpret_cast<uint32_t*>(smem + lay.qf);
-    const int nz = (lay.mrun - lay.qf) / 4;     // QF, QRF, Qsum, QRS, Ps, Pa, red
+    const int nz = (lay.mrun - lay.qf) / 4;
     for (int i = threadIdx.x; i < nz; i += blockDim.x) z32[i] = 0u;
     for (int i = threadIdx.x; i < NQP; i += blockDim.x) mrun[i] = -INFINITY;
   }
@@ -140,11 +179,12 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
       s1 += __shfl_xor_sync(RQ_FULL_MASK, s1, o);
       s2 += __shfl_xor_sync(RQ_FULL_MASK, s2, o);
     }
-    const int ri = (real && l != a.L - 1) ? l - blk.r0 : -1;
+    const int ri = col_ri(n);
+    const int bits = ri >= 0 ? a.rbits[ri] : 0;
     const int grp = (lane * P) >> 5;
     if ((lane & (32 / P - 1)) == 0) {
       Qsum[grp * NQP + n] = s1;
-      if (ri >= 0) QRS[(ri * NG + grp) * 8 + (n & 7)] = s2;
+      if (ri >= 0) QRsum[grp * NQP + n] = s2;
     }
     const int nt = n >> 3, nn = n & 7;
 #pragma unroll
@@ -152,22 +192,20 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
       const int ch = lane * P + j, gq = ch >> 5, cl = ch & 31;
       {  // 4-bit mapping: slot (c4, s, hi, e) <- channel 8 c4 + 2 s + hi + 4 e, scale 16^-hi
         const int c4 = cl >> 3, w8 = cl & 7, s = (w8 >> 1) & 1, hi = w8 & 1, e = w8 >> 2;
-        __half* dst = reinterpret_cast<__half*>(&QF[((gq * 2 + s) * NT + nt) * 32 + nn * 4 + c4]);
-        split_half(hi ? v[j] * 0.0625f : v[j], dst[hi * 2 + e], dst[4 + hi * 2 + e]);
-      }
-      if (ri >= 0) {
-        __half* base = reinterpret_cast<__half*>(QRF);
-        if (a.rbits[ri] == 4) {
-          const int c4 = cl >> 3, w8 = cl & 7, s = (w8 >> 1) & 1, hi = w8 & 1, e = w8 >> 2;
-          __half* dst = base + (((ri * NG + gq) * 2 + s) * 32 + nn * 4 + c4) * 8;
-          split_half(hi ? rr[j] * 0.0625f : rr[j], dst[hi * 2 + e], dst[4 + hi * 2 + e]);
-        } else {  // 2-bit mapping: slot (cq, s, hi, e) <- channel 16(cq/2) + 4(cq%2) + 2s + hi + 8e
-          const int e = (cl >> 3) & 1, cq = 2 * (cl >> 4) + ((cl & 7) >> 2), jj = cl & 3;
-          const int s = jj >> 1, hi = jj & 1;
-          const float sc = (jj == 0) ? 1.f : (jj == 1) ? 0.25f : (jj == 2) ? 0.0625f : 0.015625f;
-          __half* dst = base + (((ri * NG + gq) * 2 + s) * 32 + nn * 4 + cq) * 8;
-          split_half(rr[j] * sc, dst[hi * 2 + e], dst[4 + hi * 2 + e]);
+        const int idx = ((gq * 2 + s) * NT + nt) * 32 + nn * 4 + c4;
+        __half* dq = reinterpret_cast<__half*>(&QF[idx]);
+        split_half(hi ? v[j] * 0.0625f : v[j], dq[hi * 2 + e], dq[4 + hi * 2 + e]);
+        if (RES4 && bits == 4) {
+          __half* dr = reinterpret_cast<__half*>(&QR4[idx]);
+          split_half(hi ? rr[j] * 0.0625f : rr[j], dr[hi * 2 + e], dr[4 + hi * 2 + e]);
         }
+      }
+      if (bits == 2) {  // 2-bit mapping: slot (cq, s, hi, e) <- channel 16(cq/2)+4(cq%2)+2s+hi+8e
+        const int e = (cl >> 3) & 1, cq = 2 * (cl >> 4) + ((cl & 7) >> 2), jj = cl & 3;
+        const int s = jj >> 1, hi = jj & 1;
+        const float sc = (jj == 0) ? 1.f : (jj == 1) ? 0.25f : (jj == 2) ? 0.0625f : 0.015625f;
+        __half* dr = reinterpret_cast<__half*>(&QR2[((gq * 2 + s) * NT + nt) * 32 + nn * 4 + cq]);
+        split_half(rr[j] * sc, dr[hi * 2 + e], dr[4 + hi * 2 + e]);
       }
     }
   }
@@ -195,7 +233,9 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
     bulk_g2s(dst + a.off_km, a.km + tok * NG * 2, kT * NG * 4, bar);
     bulk_g2s(dst + a.off_vc, a.vc + tok * RB4, kT * RB4, bar);
     bulk_g2s(dst + a.off_vm, a.vm + tok * NG * 2, kT * NG * 4, bar);
-    for (int ri = 0; ri < nr; ++ri) {
+#pragma unroll
+    for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
+      if (ri >= nr) break;
       const int rb = D * a.rbits[ri] / 8;
       bulk_g2s(dst + a.off_krc[ri], a.krc[ri] + tok * rb, kT * rb, bar);
       bulk_g2s(dst + a.off_krm[ri], a.krm[ri] + tok * NG * 2, kT * NG * 4, bar);
@@ -205,12 +245,29 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
       bulk_g2s(dst + a.off_va[ri], a.va[ri] + tok, kT * 2, bar);
     }
   };
-  int next_issue = 0;   // tiles issued so far (thread 0)
+  int next_issue = 0;  // tiles issued so far (thread 0)
   if (threadIdx.x == 0) {
     for (; next_issue < S && next_issue < ntiles; ++next_issue) issue(next_issue);
   }
 
-  // per-column facts for this thread's score columns (nt*8 + 2c + e)
+  // residual indices of this lane's B-fragment columns (nt*8 + r) and D-fragment columns
+  // (nt*8 + 2c + e)
+  int riB[NT], riD[NT][2];
+  int krmD[NT][2], kaD[NT][2], vaD[NT][2], vrmB[NT];   // stage offsets of those columns' loops
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    riB[nt] = col_ri(nt * 8 + r);
+    vrmB[nt] = pick_int(a.off_vrm, riB[nt] < 0 ? 0 : riB[nt]);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      riD[nt][e] = col_ri(nt * 8 + 2 * c + e);
+      const int rc = riD[nt][e] < 0 ? 0 : riD[nt][e];
+      krmD[nt][e] = pick_int(a.off_krm, rc);
+      kaD[nt][e] = pick_int(a.off_ka, rc);
+      vaD[nt][e] = pick_int(a.off_va, rc);
+    }
+  }
+
   float lpart[NT][2];
   float accR[MTW][NT][4], accE2[MTW][NT][4], accE4[RES4 ? MTW : 1][NT][4];
   float offR[NT], offE[NT];
@@ -239,6 +296,7 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
 
     // -------------------------------------------------------------- scores (16 tokens/warp)
     const int tr0 = 16 * warp + r, tr1 = tr0 + 8;
+    const bool v0 = t0 + tr0 < t_end, v1 = t0 + tr1 < t_end;
     float sc[NT][4];
     {
       float Sref[NT][4], Sres[NT][4];
@@ -246,103 +304,114 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int k = 0; k < 4; ++k) Sref[nt][k] = Sres[nt][k] = 0.f;
+      float2 mk0[NG], mk1[NG];
 #pragma unroll
       for (int gq = 0; gq < NG; ++gq) {
-        const uint32_t wl = lds32(sb + a.off_kc + tr0 * RB4 + 16 * gq + 4 * c);
-        const uint32_t wh = lds32(sb + a.off_kc + tr1 * RB4 + 16 * gq + 4 * c);
-        const float2 m0 = ld_meta(sb + a.off_km + (tr0 * NG + gq) * 4);
-        const float2 m1 = ld_meta(sb + a.off_km + (tr1 * NG + gq) * 4);
-        float Dg[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) Dg[nt][k] = 0.f;
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const uint32_t xl = s ? (wl >> 8) : wl, xh = s ? (wh >> 8) : wh;
-          const uint32_t a0 = code_pair(xl, 0x000F000Fu), a1 = code_pair(xh, 0x000F000Fu);
-          const uint32_t a2 = code_pair(xl, 0x00F000F0u), a3 = code_pair(xh, 0x00F000F0u);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint4 bq = QF[((gq * 2 + s) * NT + nt) * 32 + lane];
-            mma_f16(Dg[nt], a0, a1, a2, a3, bq.x, bq.y);
-            mma_f16(Dg[nt], a0, a1, a2, a3, bq.z, bq.w);
-          }
-        }
-        const float s0 = m0.x * kCodeUnit, s1 = m1.x * kCodeUnit;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float2 qs = *reinterpret_cast<const float2*>(&Qsum[gq * NQP + nt * 8 + 2 * c]);
-          Sref[nt][0] += s0 * Dg[nt][0] + m0.y * qs.x;
-          Sref[nt][1] += s0 * Dg[nt][1] + m0.y * qs.y;
-          Sref[nt][2] += s1 * Dg[nt][2] + m1.y * qs.x;
-          Sref[nt][3] += s1 * Dg[nt][3] + m1.y * qs.y;
-        }
+        mk0[gq] = ld_meta(sb + a.off_km + (tr0 * NG + gq) * 4);
+        mk1[gq] = ld_meta(sb + a.off_km + (tr1 * NG + gq) * 4);
       }
-      for (int ri = 0; ri < nr; ++ri) {
-        const int l = blk.r0 + ri;
-        const int nt_ri = ((l - blk.lb) * blk.gw) >> 3;
-        const bool two = a.rbits[ri] == 2;
 #pragma unroll
-        for (int gq = 0; gq < NG; ++gq) {
-          uint32_t wl, wh;
-          if (two) {
-            const int off = a.off_krc[ri] + 8 * gq + 4 * (c >> 1);
-            wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
-            wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
-          } else {
-            wl = lds32(sb + a.off_krc[ri] + tr0 * RB4 + 16 * gq + 4 * c);
-            wh = lds32(sb + a.off_krc[ri] + tr1 * RB4 + 16 * gq + 4 * c);
-          }
-          const float2 m0 = ld_meta(sb + a.off_krm[ri] + (tr0 * NG + gq) * 4);
-          const float2 m1 = ld_meta(sb + a.off_krm[ri] + (tr1 * NG + gq) * 4);
-          float Dg[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int gq = 0; gq < NG; ++gq) {
+        // reference
+        {
+          const uint32_t wl = lds32(sb + a.off_kc + tr0 * RB4 + 16 * gq + 4 * c);
+          const uint32_t wh = lds32(sb + a.off_kc + tr1 * RB4 + 16 * gq + 4 * c);
+          float Dg[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) Dg[nt][k] = 0.f;
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
-            uint32_t a0, a1, a2, a3;
-            if (two) {
-              const uint32_t mlo = 0x00030003u << (4 * s), mhi = 0x00030003u << (4 * s + 2);
-              a0 = code_pair(wl, mlo);
-              a1 = code_pair(wh, mlo);
-              a2 = code_pair(wl, mhi);
-              a3 = code_pair(wh, mhi);
-            } else {
-              const uint32_t xl = s ? (wl >> 8) : wl, xh = s ? (wh >> 8) : wh;
-              a0 = code_pair(xl, 0x000F000Fu);
-              a1 = code_pair(xh, 0x000F000Fu);
-              a2 = code_pair(xl, 0x00F000F0u);
-              a3 = code_pair(xh, 0x00F000F0u);
+            uint32_t a0, a2, a1, a3;
+            a_pairs_4bit(wl, s, a0, a2);
+            a_pairs_4bit(wh, s, a1, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint4 bq = QF[((gq * 2 + s) * NT + nt) * 32 + lane];
+              mma_f16(Dg[nt], a0, a1, a2, a3, bq.x, bq.y);
+              mma_f16(Dg[nt], a0, a1, a2, a3, bq.z, bq.w);
             }
-            const uint4 bq = QRF[((ri * NG + gq) * 2 + s) * 32 + lane];
-            mma_f16(Dg, a0, a1, a2, a3, bq.x, bq.y);
-            mma_f16(Dg, a0, a1, a2, a3, bq.z, bq.w);
           }
-          const float2 qs = *reinterpret_cast<const float2*>(&QRS[(ri * NG + gq) * 8 + 2 * c]);
-          const float s0 = m0.x * kCodeUnit, s1 = m1.x * kCodeUnit;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            if (nt != nt_ri) continue;
-            Sres[nt][0] += s0 * Dg[0] + m0.y * qs.x;
-            Sres[nt][1] += s0 * Dg[1] + m0.y * qs.y;
-            Sres[nt][2] += s1 * Dg[2] + m1.y * qs.x;
-            Sres[nt][3] += s1 * Dg[3] + m1.y * qs.y;
+            const float2 qs = *reinterpret_cast<const float2*>(&Qsum[gq * NQP + nt * 8 + 2 * c]);
+            Sref[nt][0] += mk0[gq].x * Dg[nt][0] + mk0[gq].y * qs.x;
+            Sref[nt][1] += mk0[gq].x * Dg[nt][1] + mk0[gq].y * qs.y;
+            Sref[nt][2] += mk1[gq].x * Dg[nt][2] + mk1[gq].y * qs.x;
+            Sref[nt][3] += mk1[gq].x * Dg[nt][3] + mk1[gq].y * qs.y;
+          }
+        }
+        // residuals of every loop of the block, one fragment
+        if (nr > 0) {
+          float Dr[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) Dr[nt][k] = 0.f;
+#pragma unroll
+          for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
+            if (ri >= nr) break;
+            const int nt_ri = ((blk.r0 + ri - blk.lb) * blk.gw) >> 3;
+            const bool two = a.rbits[ri] == 2;
+            uint32_t wl, wh;
+            if (two) {
+              const int off = a.off_krc[ri] + 8 * gq + 4 * (c >> 1);
+              wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
+              wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
+            } else {
+              wl = lds32(sb + a.off_krc[ri] + tr0 * RB4 + 16 * gq + 4 * c);
+              wh = lds32(sb + a.off_krc[ri] + tr1 * RB4 + 16 * gq + 4 * c);
+            }
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              uint32_t a0, a1, a2, a3;
+              if (two) {
+                a_pairs_2bit(wl, s, a0, a2);
+                a_pairs_2bit(wh, s, a1, a3);
+              } else {
+                a_pairs_4bit(wl, s, a0, a2);
+                a_pairs_4bit(wh, s, a1, a3);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (nt != nt_ri) continue;
+                const int fi = ((gq * 2 + s) * NT + nt) * 32 + lane;
+                const uint4 bq = sel4(riB[nt] == ri, (RES4 && !two) ? QR4[fi] : QR2[fi]);
+                mma_f16(Dr[nt], a0, a1, a2, a3, bq.x, bq.y);
+                mma_f16(Dr[nt], a0, a1, a2, a3, bq.z, bq.w);
+              }
+            }
+          }
+          // each column's own loop: its step and offset
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int ri = riD[nt][e];
+              const float2 m0 = ld_meta(sb + krmD[nt][e] + (tr0 * NG + gq) * 4);
+              const float2 m1 = ld_meta(sb + krmD[nt][e] + (tr1 * NG + gq) * 4);
+              const float qrs = QRsum[gq * NQP + nt * 8 + 2 * c + e];
+              const float d0 = m0.x * Dr[nt][e] + m0.y * qrs;
+              const float d1 = m1.x * Dr[nt][2 + e] + m1.y * qrs;
+              Sres[nt][e] += ri >= 0 ? d0 : 0.f;
+              Sres[nt][2 + e] += ri >= 0 ? d1 : 0.f;
+            }
           }
         }
       }
-      // combine: score = a_t * ref part + residual part (final loop: the reference alone)
-      const bool v0 = t0 + tr0 < t_end, v1 = t0 + tr1 < t_end;
+      // score = a_t * reference part + residual part (final loop: the reference alone)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int col = nt * 8 + 2 * c + e;
-          const int li = col / blk.gw;
-          const int l = blk.lb + li;
+          const int ri = riD[nt][e];
           float s_0 = Sref[nt][e], s_1 = Sref[nt][2 + e];
-          if (li < blk.nl && l != a.L - 1) {
-            const int ri = l - blk.r0;
-            s_0 = ld_half(sb + a.off_ka[ri] + tr0 * 2) * s_0 + Sres[nt][e];
-            s_1 = ld_half(sb + a.off_ka[ri] + tr1 * 2) * s_1 + Sres[nt][2 + e];
+          if (nr > 0) {
+            const float al0 = ld_half(sb + kaD[nt][e] + tr0 * 2);
+            const float al1 = ld_half(sb + kaD[nt][e] + tr1 * 2);
+            s_0 = ri >= 0 ? al0 * s_0 + Sres[nt][e] : s_0;
+            s_1 = ri >= 0 ? al1 * s_1 + Sres[nt][2 + e] : s_1;
           }
           sc[nt][e] = v0 ? s_0 : -INFINITY;
           sc[nt][2 + e] = v1 ? s_1 : -INFINITY;
@@ -377,8 +446,7 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
       for (int w = 1; w < kW; ++w) mt = fmaxf(mt, red[w * NQP + threadIdx.x]);
       mnew_mine = fmaxf(mrun[threadIdx.x], mt);
     }
-    const bool v0 = t0 + tr0 < t_end, v1 = t0 + tr1 < t_end;
-    // rescale of the value-offset sums, kept per B-fragment column nt*8 + r
+    // value-offset sums are kept per B-fragment column nt*8 + r
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int col = nt * 8 + r;
@@ -403,18 +471,18 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
         corr[nt][e] = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
         const float p0 = exp2f(sc[nt][e] - mn), p1 = exp2f(sc[nt][2 + e] - mn);
         lpart[nt][e] = lpart[nt][e] * corr[nt][e] + p0 + p1;
-        const int li = col / blk.gw;
-        const int l = blk.lb + li;
+        const int ri = riD[nt][e];
         float a0v = 1.f, a1v = 1.f;
-        if (li < blk.nl && l != a.L - 1) {
-          const int ri = l - blk.r0;
-          a0v = ld_half(sb + a.off_va[ri] + tr0 * 2);
-          a1v = ld_half(sb + a.off_va[ri] + tr1 * 2);
+        if (nr > 0) {
+          const float x0 = ld_half(sb + vaD[nt][e] + tr0 * 2);
+          const float x1 = ld_half(sb + vaD[nt][e] + tr1 * 2);
+          a0v = ri >= 0 ? x0 : 1.f;
+          a1v = ri >= 0 ? x1 : 1.f;
         }
-        Ps[tr0 * NQP + col] = p0;
-        Ps[tr1 * NQP + col] = p1;
-        Pa[tr0 * NQP + col] = v0 ? p0 * a0v : 0.f;
-        Pa[tr1 * NQP + col] = v1 ? p1 * a1v : 0.f;
+        Ps[tr0 * PR + col] = v0 ? p0 : 0.f;
+        Ps[tr1 * PR + col] = v1 ? p1 : 0.f;
+        Pa[tr0 * PR + col] = v0 ? p0 * a0v : 0.f;
+        Pa[tr1 * PR + col] = v1 ? p1 * a1v : 0.f;
       }
     }
     // the stage read by tile i-1 is free (every warp is past barrier A): refill it
@@ -438,21 +506,17 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
         }
 #pragma unroll
     for (int ks = 0; ks < kT / 16; ++ks) {
-      const int tt[4] = {16 * ks + 2 * c, 16 * ks + 2 * c + 1, 16 * ks + 2 * c + 8,
-                         16 * ks + 2 * c + 9};
-      bool val[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) val[k] = t0 + tt[k] < t_end;
+      int tt[4];
+      tt[0] = 16 * ks + 2 * c;
+      tt[1] = tt[0] + 1;
+      tt[2] = tt[0] + 8;
+      tt[3] = tt[0] + 9;
       const int p0 = 8 * ks + c, p1 = p0 + 4;            // token pairs of this k-step
       // reference values
       {
-        float vs[4], vz[4];
+        float2 vm[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 mm = ld_meta(sb + a.off_vm + (tt[k] * NG + gv) * 4);
-          vs[k] = mm.x;
-          vz[k] = mm.y;
-        }
+        for (int k = 0; k < 4; ++k) vm[k] = ld_meta(sb + a.off_vm + (tt[k] * NG + gv) * 4);
         uint32_t bR[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -460,9 +524,9 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
           float w[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float pa = Pa[tt[k] * NQP + n];
-            w[k] = val[k] ? pa * vs[k] : 0.f;
-            offR[nt] += val[k] ? pa * vz[k] : 0.f;
+            const float pa = Pa[tt[k] * PR + n];     // 0 for tokens past the context
+            w[k] = pa * vm[k].x;
+            offR[nt] += pa * vm[k].y;
           }
           split_half2(w[0], w[1], bR[nt][0], bR[nt][2]);
           split_half2(w[2], w[3], bR[nt][1], bR[nt][3]);
@@ -472,9 +536,9 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
 #pragma unroll
         for (int m = 0; m < MTW; ++m) {
           const int mtg = (D == 128) ? m : (warp & 1);
-          const uint32_t x0 = mtg ? (W0 >> 8) : W0, x1 = mtg ? (W1 >> 8) : W1;
-          const uint32_t a0 = code_pair(x0, 0x000F000Fu), a1 = code_pair(x0, 0x00F000F0u);
-          const uint32_t a2 = code_pair(x1, 0x000F000Fu), a3 = code_pair(x1, 0x00F000F0u);
+          uint32_t a0, a1, a2, a3;
+          a_pairs_4bit(W0, mtg, a0, a1);
+          a_pairs_4bit(W1, mtg, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma_f16(accR[m][nt], a0, a1, a2, a3, bR[nt][0], bR[nt][1]);
@@ -482,60 +546,64 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
           }
         }
       }
-      // residual values of each loop in the block
-      for (int ri = 0; ri < nr; ++ri) {
-        const int l = blk.r0 + ri;
-        const int nt_ri = ((l - blk.lb) * blk.gw) >> 3;
-        const int n = nt_ri * 8 + r;
-        const int li = n / blk.gw;
-        const bool mine = li < blk.nl && blk.lb + li == l;
-        float w[4];
+      // residual values: one set of weights per column (its own loop's step)
+      if (nr > 0) {
+        uint4 bE[NT];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 mm = ld_meta(sb + a.off_vrm[ri] + (tt[k] * NG + gv) * 4);
-          const float ps = Ps[tt[k] * NQP + n];
-          const bool use = mine && val[k];
-          w[k] = use ? ps * mm.x : 0.f;
-          const float oz = use ? ps * mm.y : 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+          const int n = nt * 8 + r;
+          const int ri = riB[nt];
+          float w[4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            if (nt == nt_ri) offE[nt] += oz;
-        }
-        uint32_t b0, b1, b0l, b1l;
-        split_half2(w[0], w[1], b0, b0l);
-        split_half2(w[2], w[3], b1, b1l);
-        if (a.rbits[ri] == 2) {
-          const int sh = 8 * (r & 1);
-          const uint32_t W0 = lds32(sb + a.off_vrc[ri] + p0 * (2 * RB2) + (4 * gv + (r >> 1)) * 4) >> sh;
-          const uint32_t W1 = lds32(sb + a.off_vrc[ri] + p1 * (2 * RB2) + (4 * gv + (r >> 1)) * 4) >> sh;
-#pragma unroll
-          for (int m = 0; m < MTW; ++m) {
-            const int mtg = (D == 128) ? m : (warp & 1);
-            const uint32_t mlo = 0x00030003u << (4 * mtg), mhi = 0x00030003u << (4 * mtg + 2);
-            const uint32_t a0 = code_pair(W0, mlo), a1 = code_pair(W0, mhi);
-            const uint32_t a2 = code_pair(W1, mlo), a3 = code_pair(W1, mhi);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              if (nt == nt_ri) {
-                mma_f16(accE2[m][nt], a0, a1, a2, a3, b0, b1);
-                mma_f16(accE2[m][nt], a0, a1, a2, a3, b0l, b1l);
-              }
+          for (int k = 0; k < 4; ++k) {
+            const float2 mm = ld_meta(sb + vrmB[nt] + (tt[k] * NG + gv) * 4);
+            const float ps = ri >= 0 ? Ps[tt[k] * PR + n] : 0.f;
+            w[k] = ps * mm.x;
+            offE[nt] += ps * mm.y;
           }
-        } else if (RES4) {
-          const uint32_t W0 = lds32(sb + a.off_vrc[ri] + p0 * D + (8 * gv + r) * 4);
-          const uint32_t W1 = lds32(sb + a.off_vrc[ri] + p1 * D + (8 * gv + r) * 4);
+          split_half2(w[0], w[1], bE[nt].x, bE[nt].z);
+          split_half2(w[2], w[3], bE[nt].y, bE[nt].w);
+        }
 #pragma unroll
-          for (int m = 0; m < MTW; ++m) {
-            const int mtg = (D == 128) ? m : (warp & 1);
-            const uint32_t x0 = mtg ? (W0 >> 8) : W0, x1 = mtg ? (W1 >> 8) : W1;
-            const uint32_t a0 = code_pair(x0, 0x000F000Fu), a1 = code_pair(x0, 0x00F000F0u);
-            const uint32_t a2 = code_pair(x1, 0x000F000Fu), a3 = code_pair(x1, 0x00F000F0u);
+        for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
+          if (ri >= nr) break;
+          const int nt_ri = ((blk.r0 + ri - blk.lb) * blk.gw) >> 3;
+          if (a.rbits[ri] == 2) {
+            const int sh = 8 * (r & 1);
+            const int ub = (4 * gv + (r >> 1)) * 4;
+            const uint32_t W0 = lds32(sb + a.off_vrc[ri] + p0 * (2 * RB2) + ub) >> sh;
+            const uint32_t W1 = lds32(sb + a.off_vrc[ri] + p1 * (2 * RB2) + ub) >> sh;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              if (nt == nt_ri) {
-                mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, b0, b1);
-                mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, b0l, b1l);
+            for (int m = 0; m < MTW; ++m) {
+              const int mtg = (D == 128) ? m : (warp & 1);
+              uint32_t a0, a1, a2, a3;
+              a_pairs_2bit(W0, mtg, a0, a1);
+              a_pairs_2bit(W1, mtg, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (nt != nt_ri) continue;
+                const uint4 bb = sel4(riB[nt] == ri, bE[nt]);
+                mma_f16(accE2[m][nt], a0, a1, a2, a3, bb.x, bb.y);
+                mma_f16(accE2[m][nt], a0, a1, a2, a3, bb.z, bb.w);
               }
+            }
+          } else if (RES4) {
+            const uint32_t W0 = lds32(sb + a.off_vrc[ri] + p0 * D + (8 * gv + r) * 4);
+            const uint32_t W1 = lds32(sb + a.off_vrc[ri] + p1 * D + (8 * gv + r) * 4);
+#pragma unroll
+            for (int m = 0; m < MTW; ++m) {
+              const int mtg = (D == 128) ? m : (warp & 1);
+              uint32_t a0, a1, a2, a3;
+              a_pairs_4bit(W0, mtg, a0, a1);
+              a_pairs_4bit(W1, mtg, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (nt != nt_ri) continue;
+                const uint4 bb = sel4(riB[nt] == ri, bE[nt]);
+                mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, bb.x, bb.y);
+                mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, bb.z, bb.w);
+              }
+            }
           }
         }
       }
@@ -609,8 +677,8 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {      // hh: row r (j even) or row r+8 (j odd)
           const int j = 2 * mtg + hh;
-          const float sc4 = (j & 1) ? kCodeUnit / 16.f : kCodeUnit;
-          const float sc2 = kCodeUnit / float(1 << (2 * j));
+          const float sc4 = (j & 1) ? 0.0625f : 1.f;
+          const float sc2 = 1.f / float(1 << (2 * j));
           const float vr = accR[m][nt][2 * hh + e] * sc4 + oR;
           float ve = accE2[m][nt][2 * hh + e] * sc2 + oE;
           if (RES4) ve += accE4[RES4 ? m : 0][nt][2 * hh + e] * sc4;
@@ -622,32 +690,111 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
   }
 }
 
-template <int D, int NT, bool RES4>
-cudaError_t launch_variant(const MmaArgs& a, dim3 grid, size_t smem, cudaStream_t stream) {
-  auto k = rq_mma_kernel<D, NT, RES4>;
-  // opt in to the largest dynamic shared memory once per kernel variant and device
+using KernelFn = void (*)(MmaArgs);
+
+template <int D>
+KernelFn pick_kernel(int nt, bool res4) {
+  if (nt == 1) return res4 ? rq_mma_kernel<D, 1, true> : rq_mma_kernel<D, 1, false>;
+  if (nt == 2) return res4 ? rq_mma_kernel<D, 2, true> : rq_mma_kernel<D, 2, false>;
+  return res4 ? rq_mma_kernel<D, 4, true> : rq_mma_kernel<D, 4, false>;
+}
+
+KernelFn pick(int D, int nt, bool res4) {
+  return D == 128 ? pick_kernel<128>(nt, res4) : pick_kernel<64>(nt, res4);
+}
+
+// Opt every kernel variant in to the largest dynamic shared memory, once per device.
+cudaError_t prepare_kernels() {
   static std::once_flag once[64];
-  static cudaError_t set_err[64];
+  static cudaError_t err[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::call_once(once[dev], [&] {
-    set_err[dev] = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    err[dev] = cudaSuccess;
+    for (int D : {64, 128})
+      for (int nt : {1, 2, 4})
+        for (bool r4 : {false, true}) {
+          cudaError_t e = cudaFuncSetAttribute(pick(D, nt, r4),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               200 * 1024);
+          if (e != cudaSuccess) err[dev] = e;
+        }
   });
-  if (set_err[dev] != cudaSuccess) return set_err[dev];
-  k<<<grid, kW * 32, smem, stream>>>(a);
-  return cudaGetLastError();
+  return err[dev];
 }
 
-template <int D>
-cudaError_t launch_d(const MmaArgs& a, int nt, bool res4, dim3 grid, size_t smem,
-                     cudaStream_t stream) {
-  if (nt == 1) return res4 ? launch_variant<D, 1, true>(a, grid, smem, stream)
-                           : launch_variant<D, 1, false>(a, grid, smem, stream);
-  if (nt == 2) return res4 ? launch_variant<D, 2, true>(a, grid, smem, stream)
-                           : launch_variant<D, 2, false>(a, grid, smem, stream);
-  return res4 ? launch_variant<D, 4, true>(a, grid, smem, stream)
-              : launch_variant<D, 4, false>(a, grid, smem, stream);
+// CTAs of a kernel variant resident per SM with `smem` bytes of dynamic shared memory.
+int resident_ctas(int D, int nt, bool res4, size_t smem) {
+  int n = 0;
+  if (prepare_kernels() == cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, nt, res4), kW * 32, smem) ==
+          cudaSuccess &&
+      n > 0)
+    return n;
+  const int by_smem = int((227 * 1024) / (smem + 1024));   // no device: shared-memory bound
+  return by_smem < 1 ? 1 : (by_smem > 8 ? 8 : by_smem);
 }
+
+struct BlockLaunch {
+  MmaArgs a;
+  int nt;
+  bool res4;
+  size_t smem;
+};
+
+// Arguments, stage layout and shared memory of one query block (no launch).
+bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq, BlockLaunch& bl) {
+  MmaArgs& a = bl.a;
+  memset(&a, 0, sizeof(a));
+  const int D = s.head_dim, NG = D / 32;
+  a.kc = cache.ref_codes[0];
+  a.km = cache.ref_meta[0];
+  a.vc = cache.ref_codes[1];
+  a.vm = cache.ref_meta[1];
+  int off = 0;
+  a.off_kc = off; off += kT * D / 2;
+  a.off_km = off; off += kT * NG * 4;
+  a.off_vc = off; off += kT * D / 2;
+  a.off_vm = off; off += kT * NG * 4;
+  bool res4 = false;
+  for (int ri = 0; ri < bq.nr; ++ri) {
+    const int l = bq.r0 + ri;
+    const int bits = s.res_bits[l];
+    res4 |= bits == 4;
+    a.rbits[ri] = bits;
+    a.krc[ri] = cache.res_codes[0][l];
+    a.krm[ri] = cache.res_meta[0][l];
+    a.ka[ri] = cache.alpha[0][l];
+    a.vrc[ri] = cache.res_codes[1][l];
+    a.vrm[ri] = cache.res_meta[1][l];
+    a.va[ri] = cache.alpha[1][l];
+    a.off_krc[ri] = off; off += kT * D * bits / 8;
+    a.off_krm[ri] = off; off += kT * NG * 4;
+    a.off_ka[ri] = off;  off += kT * 2;
+    a.off_vrc[ri] = off; off += kT * D * bits / 8;
+    a.off_vrm[ri] = off; off += kT * NG * 4;
+    a.off_va[ri] = off;  off += kT * 2;
+  }
+  a.stage_bytes = off;
+  a.blk = bq;
+  const int nq = bq.gw * bq.nl;
+  bl.nt = nq <= 8 ? 1 : (nq <= 16 ? 2 : 4);
+  bl.res4 = res4;
+  // most resident CTAs per SM first (latency hiding), then the deepest pipeline
+  int best_ctas = 0;
+  for (int stages = 3; stages >= 2; --stages) {
+    const size_t sm = smem_layout(D, bl.nt, res4, stages, a.stage_bytes).total;
+    if (sm > 200 * 1024) continue;
+    const int ctas = resident_ctas(D, bl.nt, res4, sm);
+    if (ctas > best_ctas) {
+      best_ctas = ctas;
+      a.n_stages = stages;
+      bl.smem = sm;
+    }
+  }
+  return best_ctas > 0;
+}
+
 
 }  // namespace
 
@@ -681,57 +828,38 @@ int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* 
   return n;
 }
 
-size_t stage_bytes_for(int D, const int8_t* res_bits, const QueryBlock& bq) {
-  const int NG = D / 32;
-  size_t s = 2 * (size_t(kT) * D / 2 + size_t(kT) * NG * 4);
-  for (int ri = 0; ri < bq.nr; ++ri)
-    s += 2 * (size_t(kT) * D * res_bits[bq.r0 + ri] / 8 + size_t(kT) * NG * 4 + kT * 2);
-  return s;
+SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int max_ctx) {
+  // the resident CTAs per SM follow the largest shared-memory block of the call
+  QueryBlock blocks[64];
+  const int g = s.n_q_heads / s.n_kv_heads;
+  const int nb = plan_query_blocks(g, loop_begin, loop_count, s.n_loops, blocks, 64);
+  rq_cache dummy;
+  memset(&dummy, 0, sizeof(dummy));
+  int ctas = 0;
+  for (int i = 0; i < nb; ++i) {
+    BlockLaunch bl;
+    if (!build_block(s, dummy, blocks[i], bl)) continue;
+    const int n = resident_ctas(s.head_dim, bl.nt, bl.res4, bl.smem);
+    if (ctas == 0 || n < ctas) ctas = n;
+  }
+  return plan_splits_for(s, max_ctx, ctas > 0 ? ctas : 1, kT);
 }
 
 cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const uint16_t* q,
                                  int loop_begin, int loop_count, const int32_t* ctx_lens,
                                  int n_splits, int tokens_per_split, float* part, unsigned* err,
                                  cudaStream_t stream) {
+  cudaError_t e = prepare_kernels();
+  if (e != cudaSuccess) return e;
   QueryBlock blocks[64];
   const int g = s.n_q_heads / s.n_kv_heads;
   const int nb = plan_query_blocks(g, loop_begin, loop_count, s.n_loops, blocks, 64);
   if (nb < 0) return cudaErrorInvalidConfiguration;
-  const int D = s.head_dim, NG = D / 32;
-  const float scale = s.softmax_scale > 0.f ? s.softmax_scale : 1.0f / sqrtf(float(D));
+  const float scale = s.softmax_scale > 0.f ? s.softmax_scale : 1.0f / sqrtf(float(s.head_dim));
   for (int bi = 0; bi < nb; ++bi) {
-    const QueryBlock& bq = blocks[bi];
-    MmaArgs a;
-    memset(&a, 0, sizeof(a));
-    a.kc = cache.ref_codes[0];
-    a.km = cache.ref_meta[0];
-    a.vc = cache.ref_codes[1];
-    a.vm = cache.ref_meta[1];
-    int off = 0;
-    a.off_kc = off; off += kT * D / 2;
-    a.off_km = off; off += kT * NG * 4;
-    a.off_vc = off; off += kT * D / 2;
-    a.off_vm = off; off += kT * NG * 4;
-    bool res4 = false;
-    for (int ri = 0; ri < bq.nr; ++ri) {
-      const int l = bq.r0 + ri;
-      const int bits = s.res_bits[l];
-      res4 |= bits == 4;
-      a.rbits[ri] = bits;
-      a.krc[ri] = cache.res_codes[0][l];
-      a.krm[ri] = cache.res_meta[0][l];
-      a.ka[ri] = cache.alpha[0][l];
-      a.vrc[ri] = cache.res_codes[1][l];
-      a.vrm[ri] = cache.res_meta[1][l];
-      a.va[ri] = cache.alpha[1][l];
-      a.off_krc[ri] = off; off += kT * D * bits / 8;
-      a.off_krm[ri] = off; off += kT * NG * 4;
-      a.off_ka[ri] = off; off += kT * 2;
-      a.off_vrc[ri] = off; off += kT * D * bits / 8;
-      a.off_vrm[ri] = off; off += kT * NG * 4;
-      a.off_va[ri] = off; off += kT * 2;
-    }
-    a.stage_bytes = off;
+    BlockLaunch bl;
+    if (!build_block(s, cache, blocks[bi], bl)) return cudaErrorInvalidConfiguration;
+    MmaArgs& a = bl.a;
     a.ksigns = cache.rot_signs[0];
     a.q = q;
     a.ctx_lens = ctx_lens;
@@ -747,21 +875,10 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.loop_count = loop_count;
     a.n_splits = n_splits;
     a.tokens_per_split = tokens_per_split;
-    a.blk = bq;
     a.scale_log2 = scale * kLog2e;
-    const int nq = bq.gw * bq.nl;
-    const int nt = nq <= 8 ? 1 : (nq <= 16 ? 2 : 4);
-    int stages = 3;
-    size_t smem = 0;
-    for (; stages >= 1; --stages) {
-      smem = smem_layout(D, nt, bq.nr, stages, a.stage_bytes).total;
-      if (smem <= 200 * 1024) break;
-    }
-    if (stages < 1) return cudaErrorInvalidConfiguration;
-    a.n_stages = stages;
     dim3 grid(n_splits, s.n_kv_heads, s.batch);
-    cudaError_t e = (D == 128) ? launch_d<128>(a, nt, res4, grid, smem, stream)
-                               : launch_d<64>(a, nt, res4, grid, smem, stream);
+    pick(s.head_dim, bl.nt, bl.res4)<<<grid, kW * 32, bl.smem, stream>>>(a);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

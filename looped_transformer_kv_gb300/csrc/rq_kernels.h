@@ -17,27 +17,32 @@ struct QueryBlock {
   int gi0, gw, lb, nl, r0, nr;
 };
 
-// Shared-memory layout of the tensor-core decode kernel (byte offsets).
+// Shared-memory layout of the tensor-core decode kernel (byte offsets).  Rows of the
+// softmax-weight tables are padded by 4 floats so the value-phase fragment loads of the 4
+// token lanes of a column fall in distinct banks.
 struct SmemLayout {
-  int qf, qrf, qsum, qrs, ps, pa, red, mrun, bars, total;
+  int qf, qr2, qr4, qsum, qrsum, ps, pa, red, mrun, bars, total, prow;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int D, int NT, int nr, int stages,
+__host__ __device__ inline SmemLayout smem_layout(int D, int NT, bool res4, int stages,
                                                   int stage_bytes) {
   const int NG = D / 32, NQP = NT * 8;
   SmemLayout s;
+  s.prow = NQP + 4;
   int o = stages * stage_bytes;
   o = (o + 15) & ~15;
-  s.qf = o;   o += NG * 2 * NT * 32 * 16;   // hi and lo f16x2 pairs per lane
-  s.qrf = o;  o += nr * NG * 2 * 32 * 16;
-  s.qsum = o; o += NG * NQP * 4;
-  s.qrs = o;  o += nr * NG * 8 * 4;
-  s.ps = o;   o += 64 * NQP * 4;
-  s.pa = o;   o += 64 * NQP * 4;
-  s.red = o;  o += 4 * NQP * 4;
-  s.mrun = o; o += NQP * 4;
+  const int frag = NG * 2 * NT * 32 * 16;   // hi and lo f16x2 pairs per lane
+  s.qf = o;    o += frag;
+  s.qr2 = o;   o += frag;
+  s.qr4 = o;   o += res4 ? frag : 0;
+  s.qsum = o;  o += NG * NQP * 4;
+  s.qrsum = o; o += NG * NQP * 4;
+  s.ps = o;    o += 64 * s.prow * 4;
+  s.pa = o;    o += 64 * s.prow * 4;
+  s.red = o;   o += 4 * NQP * 4;
+  s.mrun = o;  o += NQP * 4;
   o = (o + 7) & ~7;
-  s.bars = o; o += stages * 8;
+  s.bars = o;  o += stages * 8;
   s.total = o;
   return s;
 }
@@ -57,6 +62,11 @@ struct SplitPlan {
   int tokens_per_split;  // multiple of the kernel's token chunk
 };
 
+// Split-KV plan for a kernel that keeps `ctas_per_sm` CTAs resident per SM and moves
+// `chunk`-token tiles: the number of splits minimises (waves) x (tiles per split + set-up).
+SplitPlan plan_splits_for(const rq_shape& s, int max_ctx, int ctas_per_sm, int chunk);
+SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int max_ctx);
+SplitPlan plan_splits_bf16(const rq_shape& s, int max_ctx);
 SplitPlan plan_splits(const rq_shape& s, int loop_count, int max_ctx);
 size_t partial_floats(const rq_shape& s);  // floats of one partial record
 
