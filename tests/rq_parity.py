@@ -5,7 +5,9 @@ fp16 value (step, offset, a_l) and every code, the oracle recomputes the value; 
 GPU's value differs, it is accepted only if the two are neighbours and the oracle's
 pre-rounding value lies within 1e-6 (relative to the value for fp16 quantities, in code
 units for codes) of the boundary between them.  The oracle then continues with the GPU's
-choice.  Everything else must match bit for bit, packed bytes included.
+choice.  Everything else must match bit for bit, packed bytes included.  Reported counts:
+codes whose value lies within the band (`band`, out of `codes`) and elements where the GPU's
+neighbouring choice was taken (`followed`, out of `elements`); both stay below 1e-5.
 
 Output parity: GPU bf16 output vs the oracle's fp64 output,
     max over elements of (|gpu - ref| - ulp_bf16(ref)/2) <= 2e-3,
@@ -37,7 +39,8 @@ class Follow:
     def __init__(self, gpu):
         self.gpu = gpu
         self.total = 0
-        self.band = 0          # elements whose value lies within the band of a boundary
+        self.codes = 0         # packed codes checked
+        self.band = 0          # codes whose pre-rounding value lies within the band
         self.followed = 0      # elements where the GPU's neighbouring choice was taken
         self.bad = 0           # any other disagreement
         self.bad_names = {}
@@ -51,16 +54,15 @@ class Follow:
             band = np.abs(pre - (np.floor(pre) + 0.5)) <= CODE_BAND
             near = diff & (np.abs(g - rounded) == 1) & \
                 (np.abs(pre - (g + rounded) / 2) <= CODE_BAND)
+            self.codes += rounded.size
+            self.band += int(band.sum())
         else:
-            mid = _fp16_neighbour_mid(pre, rounded)
-            band = np.abs(pre - mid) <= REL_BAND * np.abs(pre)
             toward = np.where(g > rounded, np.float16(np.inf), np.float16(-np.inf))
             adjacent = np.nextafter(rounded.astype(np.float16),
                                     toward.astype(np.float16)).astype(np.float64) == g
             near = diff & adjacent & (np.abs(pre - (g + rounded) / 2) <= REL_BAND * np.abs(pre))
         bad = diff & ~near
         self.total += rounded.size
-        self.band += int(band.sum())
         self.followed += int(near.sum())
         nb = int(bad.sum())
         if nb:
@@ -144,7 +146,7 @@ def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True):
     x = x.astype(np.float64)                                      # [ntok][2][L][d]
     sl = w.packed_slice(b, h, ntok_e)
     signs = w.signs_np[h].astype(np.float64)                      # [2][d]
-    stats = {"elements": 0, "band": 0, "followed": 0}
+    stats = {"elements": 0, "codes": 0, "band": 0, "followed": 0}
     encs = []
     for kv in range(2):
         f = Follow(gpu_slice_to_oracle_names(sl, kv, d, L, res_bits))
@@ -153,6 +155,7 @@ def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True):
         if check_encode:
             assert packed_bytes_equal(enc, sl, kv, res_bits), "packed bytes differ kv=%d" % kv
         stats["elements"] += f.total
+        stats["codes"] += f.codes
         stats["band"] += f.band
         stats["followed"] += f.followed
         encs.append(enc_head(enc, ctx))
