@@ -33,10 +33,14 @@
  *   res_meta[kv][l]   fp16   [B][Hkv][cap][ng][2]
  *   alpha[kv][l]      fp16   [B][Hkv][cap]               least-squares scale a_l
  *   rot_signs[kv]     int8   [Hkv][d]                    +-1; R = H_d diag(signs)/sqrt(d)
- * A token's code row packs channel i into byte i*b/8 at bit offset (i*b) % 8.  K rows
- * are stored one after another.  V rows are stored in token pairs: for tokens 2p and
- * 2p+1 the 16-bit units of the two rows alternate (unit u of token 2p, unit u of token
- * 2p+1, unit u+1 of token 2p, ...).  Capacity must be a multiple of 64 (the decode kernel
+ * A token's natural code row packs channel i into byte i*b/8 at bit offset (i*b) % 8.
+ * K rows store the natural row's 32-bit words group-interleaved: natural word w (the
+ * (w % b)-th word of 32-channel group w / b) sits at word (w % b) * (d/32) + w / b.  V rows
+ * are stored in token pairs: in pair p (tokens 2p, 2p+1) the 32-bit word at position
+ * u ^ swz(p) holds 16-bit unit u of token 2p's natural row (low half) and of token 2p+1's
+ * (high half), with swz(p) = 8 (p % 4) for 32-unit rows, 8 ((p / 2) % 2) for 16-unit rows
+ * and 0 for shorter rows.  Both orders keep each lane's tensor-core operand loads in
+ * distinct shared-memory banks.  Capacity must be a multiple of 64 (the decode kernel
  * moves whole 64-token tiles).  Groups are 32 contiguous channels: original channels for the
  * reference, rotated channels for residuals.
  */

@@ -69,10 +69,26 @@ __device__ __forceinline__ void warp_fwht(float (&v)[P], int lane) {
   }
 }
 
-// Byte offset of byte k of token t's row in a V code array stored in token pairs
-// (16-bit units of tokens 2p and 2p+1 alternate), relative to the (b, h) slot base.
+// XOR applied to the 16-bit unit index in row pair p of a V code array whose rows hold
+// `units` 16-bit units: it spreads the pairs a fragment load touches over distinct banks.
+__host__ __device__ __forceinline__ int v_unit_swizzle(int64_t p, int units) {
+  return units == 32 ? int(8 * (p & 3)) : (units == 16 ? int(8 * ((p >> 1) & 1)) : 0);
+}
+
+// Byte offset of natural byte k of token t's row in a V code array stored in token pairs:
+// in pair p = t/2 the 32-bit word at position u ^ swizzle(p) holds 16-bit unit u = k/2 of
+// token 2p (low half) and of token 2p+1 (high half).  Relative to the (b, h) slot base.
 __device__ __forceinline__ int64_t vpair_offset(int64_t t, int k, int row_bytes) {
-  return (t >> 1) * (2 * row_bytes) + (k >> 1) * 4 + (t & 1) * 2 + (k & 1);
+  const int64_t p = t >> 1;
+  const int u = (k >> 1) ^ v_unit_swizzle(p, row_bytes >> 1);
+  return p * (2 * row_bytes) + u * 4 + (t & 1) * 2 + (k & 1);
+}
+
+// Byte offset, within a K code row, of natural byte k: words are group-interleaved (the
+// j-th word of every 32-channel group adjacent), word w -> (w % bits) * (d/32) + w / bits.
+__device__ __forceinline__ int k_row_offset(int k, int bits, int ng) {
+  const int w = k >> 2;
+  return ((w % bits) * ng + w / bits) * 4 + (k & 3);
 }
 
 }  // namespace rq

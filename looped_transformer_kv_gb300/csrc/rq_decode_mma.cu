@@ -64,6 +64,21 @@ __device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
 }
 
+template <int N>
+__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[N]) {
+  if constexpr (N == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+  }
+}
+
 __device__ __forceinline__ float2 ld_meta(const uint8_t* p) {  // (step, offset) fp16 pair
   return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
@@ -310,12 +325,16 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
         mk0[gq] = ld_meta(sb + a.off_km + (tr0 * NG + gq) * 4);
         mk1[gq] = ld_meta(sb + a.off_km + (tr1 * NG + gq) * 4);
       }
+      // this lane's word of every group (K rows are group-interleaved: one load)
+      uint32_t kw0[NG], kw1[NG];
+      load_words<NG>(sb + a.off_kc + tr0 * RB4 + c * NG * 4, kw0);
+      load_words<NG>(sb + a.off_kc + tr1 * RB4 + c * NG * 4, kw1);
 #pragma unroll
       for (int gq = 0; gq < NG; ++gq) {
         // reference
         {
-          const uint32_t wl = lds32(sb + a.off_kc + tr0 * RB4 + 16 * gq + 4 * c);
-          const uint32_t wh = lds32(sb + a.off_kc + tr1 * RB4 + 16 * gq + 4 * c);
+          const uint32_t wl = kw0[gq];
+          const uint32_t wh = kw1[gq];
           float Dg[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -356,12 +375,13 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
             const bool two = a.rbits[ri] == 2;
             uint32_t wl, wh;
             if (two) {
-              const int off = a.off_krc[ri] + 8 * gq + 4 * (c >> 1);
+              const int off = a.off_krc[ri] + ((c >> 1) * NG + gq) * 4;
               wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
               wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
             } else {
-              wl = lds32(sb + a.off_krc[ri] + tr0 * RB4 + 16 * gq + 4 * c);
-              wh = lds32(sb + a.off_krc[ri] + tr1 * RB4 + 16 * gq + 4 * c);
+              const int off = a.off_krc[ri] + (c * NG + gq) * 4;
+              wl = lds32(sb + off + tr0 * RB4);
+              wh = lds32(sb + off + tr1 * RB4);
             }
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
@@ -531,8 +551,8 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
           split_half2(w[0], w[1], bR[nt][0], bR[nt][2]);
           split_half2(w[2], w[3], bR[nt][1], bR[nt][3]);
         }
-        const uint32_t W0 = lds32(sb + a.off_vc + p0 * D + (8 * gv + r) * 4);
-        const uint32_t W1 = lds32(sb + a.off_vc + p1 * D + (8 * gv + r) * 4);
+        const uint32_t W0 = lds32(sb + a.off_vc + p0 * D + ((8 * gv + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
+        const uint32_t W1 = lds32(sb + a.off_vc + p1 * D + ((8 * gv + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
 #pragma unroll
         for (int m = 0; m < MTW; ++m) {
           const int mtg = (D == 128) ? m : (warp & 1);
@@ -570,9 +590,11 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
           const int nt_ri = ((blk.r0 + ri - blk.lb) * blk.gw) >> 3;
           if (a.rbits[ri] == 2) {
             const int sh = 8 * (r & 1);
-            const int ub = (4 * gv + (r >> 1)) * 4;
-            const uint32_t W0 = lds32(sb + a.off_vrc[ri] + p0 * (2 * RB2) + ub) >> sh;
-            const uint32_t W1 = lds32(sb + a.off_vrc[ri] + p1 * (2 * RB2) + ub) >> sh;
+            const int u = 4 * gv + (r >> 1);
+            const uint32_t W0 =
+                lds32(sb + a.off_vrc[ri] + p0 * (2 * RB2) + (u ^ v_unit_swizzle(p0, D / 8)) * 4) >> sh;
+            const uint32_t W1 =
+                lds32(sb + a.off_vrc[ri] + p1 * (2 * RB2) + (u ^ v_unit_swizzle(p1, D / 8)) * 4) >> sh;
 #pragma unroll
             for (int m = 0; m < MTW; ++m) {
               const int mtg = (D == 128) ? m : (warp & 1);
@@ -588,8 +610,10 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
               }
             }
           } else if (RES4) {
-            const uint32_t W0 = lds32(sb + a.off_vrc[ri] + p0 * D + (8 * gv + r) * 4);
-            const uint32_t W1 = lds32(sb + a.off_vrc[ri] + p1 * D + (8 * gv + r) * 4);
+            const uint32_t W0 =
+                lds32(sb + a.off_vrc[ri] + p0 * D + ((8 * gv + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
+            const uint32_t W1 =
+                lds32(sb + a.off_vrc[ri] + p1 * D + ((8 * gv + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
 #pragma unroll
             for (int m = 0; m < MTW; ++m) {
               const int mtg = (D == 128) ? m : (warp & 1);

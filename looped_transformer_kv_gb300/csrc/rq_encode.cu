@@ -65,6 +65,7 @@ __device__ __forceinline__ void quantize_lane(const float (&v)[P], int (&c)[P], 
 template <int P, int BITS>
 __device__ __forceinline__ void store_codes(uint8_t* slot, int64_t tok, int row_bytes, bool is_v,
                                             const int (&c)[P], int lane) {
+  // d = 32 P channels, so the number of 32-channel groups is P
   uint32_t w = 0;
 #pragma unroll
   for (int j = 0; j < P; ++j) w |= uint32_t(c[j]) << (BITS * j);
@@ -74,16 +75,19 @@ __device__ __forceinline__ void store_codes(uint8_t* slot, int64_t tok, int row_
     if ((lane & 1) == 0) {
       const int k = lane >> 1;
       uint8_t byte = uint8_t(w | (other << 4));
-      int64_t off = is_v ? vpair_offset(tok, k, row_bytes) : tok * row_bytes + k;
+      int64_t off = is_v ? vpair_offset(tok, k, row_bytes)
+                         : tok * row_bytes + k_row_offset(k, BITS, P);
       slot[off] = byte;
     }
   } else if (LANE_BITS == 8) {
     const int k = lane;
-    int64_t off = is_v ? vpair_offset(tok, k, row_bytes) : tok * row_bytes + k;
+    int64_t off = is_v ? vpair_offset(tok, k, row_bytes)
+                       : tok * row_bytes + k_row_offset(k, BITS, P);
     slot[off] = uint8_t(w);
   } else {  // 16 bits: one aligned 16-bit unit
     const int k = 2 * lane;
-    int64_t off = is_v ? vpair_offset(tok, k, row_bytes) : tok * row_bytes + k;
+    int64_t off = is_v ? vpair_offset(tok, k, row_bytes)
+                       : tok * row_bytes + k_row_offset(k, BITS, P);
     *reinterpret_cast<uint16_t*>(slot + off) = uint16_t(w);
   }
 }

@@ -286,21 +286,70 @@ def unpack_rows(rows, bits, d):
     return out.reshape(r.shape[0], d).astype(np.float64)
 
 
-def interleave_pairs(rows):
-    """V-side token-pair layout: rows [N][rb] (N even, rb even) -> [N/2][2*rb] where the
-    16-bit units of tokens 2p and 2p+1 alternate: byte (t, k) sits at offset
-    (k // 2) * 4 + (t % 2) * 2 + (k % 2) of pair t // 2."""
+def k_word_order(d, bits):
+    """Physical 32-bit word of each natural word of a K code row.
+
+    A K row stores its words group-interleaved: natural word w (channels of group w // bits,
+    k-th word of that group, k = w % bits) sits at word k * (d/32) + w // bits, so the k-th
+    words of all groups are adjacent."""
+    ng = d // GROUP
+    w = np.arange(d * bits // 32)
+    return (w % bits) * ng + w // bits
+
+
+def k_layout(rows, bits, d):
+    """Natural code rows [N][d*bits/8] -> the bytes stored for K rows."""
     r = np.asarray(rows, dtype=np.uint8)
     N, rb = r.shape
-    u = r.reshape(N // 2, 2, rb // 2, 2)                   # [pair][tok][unit][byte]
-    return np.ascontiguousarray(u.transpose(0, 2, 1, 3)).reshape(N // 2, 2 * rb)
+    words = r.reshape(N, rb // 4, 4)
+    out = np.empty_like(words)
+    out[:, k_word_order(d, bits), :] = words
+    return out.reshape(N, rb)
 
 
-def deinterleave_pairs(phys, rb):
-    p = np.asarray(phys, dtype=np.uint8)
-    P = p.shape[0]
-    u = p.reshape(P, rb // 2, 2, 2).transpose(0, 2, 1, 3)
-    return np.ascontiguousarray(u).reshape(2 * P, rb)
+def k_unlayout(stored, bits, d):
+    r = np.asarray(stored, dtype=np.uint8)
+    N, rb = r.shape
+    return r.reshape(N, rb // 4, 4)[:, k_word_order(d, bits), :].reshape(N, rb)
+
+
+def v_unit_swizzle(p, units):
+    """XOR applied to the 16-bit unit index u in the row pair p of a V code array: 8 (p mod 4)
+    for 32-unit rows, 8 ((p div 2) mod 2) for 16-unit rows, none for shorter rows."""
+    p = np.asarray(p)
+    if units == 32:
+        return 8 * (p & 3)
+    if units == 16:
+        return 8 * ((p >> 1) & 1)
+    return np.zeros_like(p)
+
+
+def v_layout(rows):
+    """V-side token-pair layout of natural code rows [N][rb] (N even, rb even) -> [N/2][2*rb]:
+    in pair p (tokens 2p, 2p+1) the 32-bit word at position u ^ swizzle(p) holds 16-bit unit u
+    of token 2p (low half) and of token 2p+1 (high half)."""
+    r = np.asarray(rows, dtype=np.uint8)
+    N, rb = r.shape
+    units = rb // 2
+    u = r.reshape(N // 2, 2, units, 2)                      # [pair][tok][unit][byte]
+    pairs = np.ascontiguousarray(u.transpose(0, 2, 1, 3))   # [pair][unit][tok][byte]
+    out = np.empty_like(pairs)
+    for p in range(N // 2):
+        pos = np.arange(units) ^ v_unit_swizzle(p, units)
+        out[p, pos] = pairs[p]
+    return out.reshape(N // 2, 2 * rb)
+
+
+def v_unlayout(stored, rb):
+    s = np.asarray(stored, dtype=np.uint8)
+    P = s.shape[0]
+    units = rb // 2
+    w = s.reshape(P, units, 2, 2)
+    pairs = np.empty_like(w)
+    for p in range(P):
+        pos = np.arange(units) ^ v_unit_swizzle(p, units)
+        pairs[p] = w[p, pos]
+    return np.ascontiguousarray(pairs.transpose(0, 2, 1, 3)).reshape(2 * P, rb)
 
 
 def cache_bytes(d, n_loops, res_bits, tokens, heads=1, batch=1):

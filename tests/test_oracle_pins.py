@@ -289,11 +289,20 @@ def test_pack_unpack_round_trip_and_bit_positions(bits):
     one[0, 5] = 1                              # channel 5 -> byte 5*b//8, bit (5*b)%8
     r = O.pack_rows(one, bits)
     assert r[0, 5 * bits // 8] == 1 << ((5 * bits) % 8) and r.sum() == r[0, 5 * bits // 8]
-    phys = O.interleave_pairs(rows)
-    assert phys[1, 0:2].tolist() == rows[2, 0:2].tolist()          # unit 0 of token 2
-    assert phys[1, 2:4].tolist() == rows[3, 0:2].tolist()          # unit 0 of token 3
-    assert phys[1, 4:6].tolist() == rows[2, 2:4].tolist()          # unit 1 of token 2
-    assert np.array_equal(O.deinterleave_pairs(phys, rows.shape[1]), rows)
+    rb = rows.shape[1]
+    units = rb // 2
+    phys = O.v_layout(rows)
+    sw = int(O.v_unit_swizzle(1, units))                        # pair 1 = tokens 2, 3
+    assert phys[1, 4 * sw:4 * sw + 2].tolist() == rows[2, 0:2].tolist()      # unit 0, token 2
+    assert phys[1, 4 * sw + 2:4 * sw + 4].tolist() == rows[3, 0:2].tolist()  # unit 0, token 3
+    u1 = 1 ^ sw
+    assert phys[1, 4 * u1:4 * u1 + 2].tolist() == rows[2, 2:4].tolist()      # unit 1, token 2
+    assert np.array_equal(O.v_unlayout(phys, rb), rows)
+    # K rows: the k-th words of all groups are adjacent
+    k = O.k_layout(rows, bits, 128)
+    ng = 4
+    assert k[0, 4:8].tolist() == rows[0, 4 * bits:4 * bits + 4].tolist()   # group 1, word 0
+    assert np.array_equal(O.k_unlayout(k, bits, 128), rows)
 
 
 @pytest.mark.parametrize("d,bits", [(64, (2, 2, 2)), (128, (4, 2, 2)), (128, (2,) * 7)])
