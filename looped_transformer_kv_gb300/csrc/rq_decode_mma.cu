@@ -10,11 +10,10 @@
 // The code dot products and the P.V products run as mma.sync m16n8k16 (f16 in, f32 acc):
 //   scores: M = 16 tokens, N = 8 query columns, K = 16 channels of one 32-channel group;
 //   values: M = 16 channels of one group, N = 8 query columns, K = 16 tokens.
-// A pair of packed codes becomes an f16x2 operand with one LOP3 and one packed subtract:
-// the code bits, masked in place, sit in the low mantissa bits of 1024 (0x6400), and
-// subtracting 1024 leaves the code times a power of two fixed by its bit position; that
-// power is folded into the query fragments (scores) or removed per output row at the end
-// (values).  The other operand (queries, softmax weights) is split into an fp16 high part
+// A pair of packed codes becomes an f16x2 operand with one AND: the code bits, masked in
+// place with a zero exponent field, are the fp16 subnormal c * 2^-24 times a power of two
+// fixed by their bit position; that power is folded into the query fragments (scores) or
+// removed per output row at the end (values), and 2^24 is restored in fp32.  The other operand (queries, softmax weights) is split into an fp16 high part
 // and an fp16 low part (two MMAs) and so carries about 22 significant bits; products are
 // exact in the fp32 accumulators.
 // Query columns of every loop share the fragments: the residual codes of loop l meet a
@@ -102,21 +101,25 @@ __device__ __forceinline__ uint4 sel4(bool keep, uint4 v) {
 // 4-bit group row (16 bytes) of one token: the A-operand pairs of k-step s for this lane's
 // word; slot order (2c, 2c+1 | 2c+8, 2c+9) <- channels (8c+2s, 8c+2s+4 | 8c+2s+1, 8c+2s+5),
 // the second pair scaled by 16.
+template <bool NORMAL = false>
 __device__ __forceinline__ void a_pairs_4bit(uint32_t w, int s, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = s ? (w >> 8) : w;
-  lo = code_pair(x, 0x000F000Fu);
-  hi = code_pair(x, 0x00F000F0u);
+  lo = NORMAL ? code_pair_normal(x, 0x000F000Fu) : code_pair(x, 0x000F000Fu);
+  hi = NORMAL ? code_pair_normal(x, 0x00F000F0u) : code_pair(x, 0x00F000F0u);
 }
 
 // 2-bit group row (8 bytes): this lane's byte-half of word c/2; k-step s uses codes 2s and
 // 2s+1 of each half (channels 16(c/2) + 4(c%2) + 2s + {0, 1} and +8), scaled by 4^(2s) and
 // 4^(2s+1).
+template <bool NORMAL = false>
 __device__ __forceinline__ void a_pairs_2bit(uint32_t x, int s, uint32_t& lo, uint32_t& hi) {
-  lo = code_pair(x, 0x00030003u << (4 * s));
-  hi = code_pair(x, 0x00030003u << (4 * s + 2));
+  const uint32_t m0 = 0x00030003u << (4 * s), m1 = 0x00030003u << (4 * s + 2);
+  lo = NORMAL ? code_pair_normal(x, m0) : code_pair(x, m0);
+  hi = NORMAL ? code_pair_normal(x, m1) : code_pair(x, m1);
 }
 
-template <int D, int NT, bool RES4>
+// NRT >= 0: the block's number of residual loops, fixed at compile time; -1: read at run time.
+template <int D, int NT, bool RES4, int NRT>
 __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NG = D / 32;
   constexpr int NQP = NT * 8;        // query columns (padded)
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
   const int r = lane >> 2, c = lane & 3;
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const QueryBlock blk = a.blk;
-  const int nr = blk.nr;
+  const int nr = NRT >= 0 ? NRT : blk.nr;
 
   const SmemLayout lay = smem_layout(D, NT, RES4, a.n_stages, a.stage_bytes);
   const int PR = lay.prow;
@@ -161,12 +164,12 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
     for (int i = threadIdx.x; i < NQP; i += blockDim.x) mrun[i] = -INFINITY;
   }
   __syncthreads();
-  for (int n = warp; n < NQP; n += kW) {
+  // query columns of this block: scaled q, rotated q' = R q, per-group sums
+  auto prep_column = [&](int n, float (&v)[P], float (&rr)[P]) -> bool {
     const int li = n / blk.gw;
     const int gi = blk.gi0 + n % blk.gw;
     const bool real = li < blk.nl && gi < a.g;
     const int l = blk.lb + li;
-    float v[P], rr[P];
     const int8_t* sg = a.ksigns + int64_t(h) * D + lane * P;
     if (real) {
       const uint16_t* qp =
@@ -182,10 +185,44 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
     for (int j = 0; j < P; ++j) rr[j] = v[j] * float(sg[j]);
     warp_fwht<P>(rr, lane);
     const float inv_sqrt_d = (D == 128) ? 0.08838834764831845f : 0.125f;
+#pragma unroll
+    for (int j = 0; j < P; ++j) rr[j] *= inv_sqrt_d;
+    return real;
+  };
+  // pass 1: the largest |q|, |q'| of the block fixes a power-of-two fragment scale 2^k with
+  // max |fragment| <= 2^14, so the low parts of the split stay normal fp16 (they meet the
+  // subnormal code operands of the score MMAs)
+  {
+    float mx = 0.f;
+    for (int n = warp; n < NQP; n += kW) {
+      float v[P], rr[P];
+      prep_column(n, v, rr);
+#pragma unroll
+      for (int j = 0; j < P; ++j) mx = fmaxf(mx, fmaxf(fabsf(v[j]), fabsf(rr[j])));
+    }
+    mx = warp_max(mx);
+    if (lane == 0) atomicMax(reinterpret_cast<unsigned*>(red), __float_as_uint(mx));
+  }
+  __syncthreads();
+  const float qmax = __uint_as_float(*reinterpret_cast<const unsigned*>(red));
+  int qexp = 0;
+  if (qmax > 0.f) {
+    frexpf(qmax, &qexp);                     // qmax < 2^qexp
+    qexp = 14 - qexp;
+    qexp = qexp < 0 ? 0 : (qexp > 40 ? 40 : qexp);
+  }
+  const float qscale = ldexpf(1.f, qexp);
+  const float code_unit = ldexpf(1.f, 24 - qexp);   // undoes 2^-24 codes and the q scale
+  __syncthreads();
+  if (threadIdx.x == 0) *reinterpret_cast<unsigned*>(red) = 0u;
+  // pass 2: fragments and group sums
+  for (int n = warp; n < NQP; n += kW) {
+    float v[P], rr[P];
+    const bool real = prep_column(n, v, rr);
+    (void)real;
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int j = 0; j < P; ++j) {
-      rr[j] *= inv_sqrt_d;
       s1 += v[j];
       s2 += rr[j];
     }
@@ -205,14 +242,15 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
 #pragma unroll
     for (int j = 0; j < P; ++j) {
       const int ch = lane * P + j, gq = ch >> 5, cl = ch & 31;
+      const float vq = v[j] * qscale, rq = rr[j] * qscale;
       {  // 4-bit mapping: slot (c4, s, hi, e) <- channel 8 c4 + 2 s + hi + 4 e, scale 16^-hi
         const int c4 = cl >> 3, w8 = cl & 7, s = (w8 >> 1) & 1, hi = w8 & 1, e = w8 >> 2;
         const int idx = ((gq * 2 + s) * NT + nt) * 32 + nn * 4 + c4;
         __half* dq = reinterpret_cast<__half*>(&QF[idx]);
-        split_half(hi ? v[j] * 0.0625f : v[j], dq[hi * 2 + e], dq[4 + hi * 2 + e]);
+        split_half(hi ? vq * 0.0625f : vq, dq[hi * 2 + e], dq[4 + hi * 2 + e]);
         if (RES4 && bits == 4) {
           __half* dr = reinterpret_cast<__half*>(&QR4[idx]);
-          split_half(hi ? rr[j] * 0.0625f : rr[j], dr[hi * 2 + e], dr[4 + hi * 2 + e]);
+          split_half(hi ? rq * 0.0625f : rq, dr[hi * 2 + e], dr[4 + hi * 2 + e]);
         }
       }
       if (bits == 2) {  // 2-bit mapping: slot (cq, s, hi, e) <- channel 16(cq/2)+4(cq%2)+2s+hi+8e
@@ -220,7 +258,7 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
         const int s = jj >> 1, hi = jj & 1;
         const float sc = (jj == 0) ? 1.f : (jj == 1) ? 0.25f : (jj == 2) ? 0.0625f : 0.015625f;
         __half* dr = reinterpret_cast<__half*>(&QR2[((gq * 2 + s) * NT + nt) * 32 + nn * 4 + cq]);
-        split_half(rr[j] * sc, dr[hi * 2 + e], dr[4 + hi * 2 + e]);
+        split_half(rq * sc, dr[hi * 2 + e], dr[4 + hi * 2 + e]);
       }
     }
   }
@@ -352,13 +390,14 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
               mma_f16(Dg[nt], a0, a1, a2, a3, bq.z, bq.w);
             }
           }
+          const float s0 = mk0[gq].x * code_unit, s1 = mk1[gq].x * code_unit;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const float2 qs = *reinterpret_cast<const float2*>(&Qsum[gq * NQP + nt * 8 + 2 * c]);
-            Sref[nt][0] += mk0[gq].x * Dg[nt][0] + mk0[gq].y * qs.x;
-            Sref[nt][1] += mk0[gq].x * Dg[nt][1] + mk0[gq].y * qs.y;
-            Sref[nt][2] += mk1[gq].x * Dg[nt][2] + mk1[gq].y * qs.x;
-            Sref[nt][3] += mk1[gq].x * Dg[nt][3] + mk1[gq].y * qs.y;
+            Sref[nt][0] += s0 * Dg[nt][0] + mk0[gq].y * qs.x;
+            Sref[nt][1] += s0 * Dg[nt][1] + mk0[gq].y * qs.y;
+            Sref[nt][2] += s1 * Dg[nt][2] + mk1[gq].y * qs.x;
+            Sref[nt][3] += s1 * Dg[nt][3] + mk1[gq].y * qs.y;
           }
         }
         // residuals of every loop of the block, one fragment
@@ -412,8 +451,8 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
               const float2 m0 = ld_meta(sb + krmD[nt][e] + (tr0 * NG + gq) * 4);
               const float2 m1 = ld_meta(sb + krmD[nt][e] + (tr1 * NG + gq) * 4);
               const float qrs = QRsum[gq * NQP + nt * 8 + 2 * c + e];
-              const float d0 = m0.x * Dr[nt][e] + m0.y * qrs;
-              const float d1 = m1.x * Dr[nt][2 + e] + m1.y * qrs;
+              const float d0 = (m0.x * code_unit) * Dr[nt][e] + m0.y * qrs;
+              const float d1 = (m1.x * code_unit) * Dr[nt][2 + e] + m1.y * qrs;
               Sres[nt][e] += ri >= 0 ? d0 : 0.f;
               Sres[nt][2 + e] += ri >= 0 ? d1 : 0.f;
             }
@@ -557,8 +596,8 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
         for (int m = 0; m < MTW; ++m) {
           const int mtg = (D == 128) ? m : (warp & 1);
           uint32_t a0, a1, a2, a3;
-          a_pairs_4bit(W0, mtg, a0, a1);
-          a_pairs_4bit(W1, mtg, a2, a3);
+          a_pairs_4bit<true>(W0, mtg, a0, a1);
+          a_pairs_4bit<true>(W1, mtg, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma_f16(accR[m][nt], a0, a1, a2, a3, bR[nt][0], bR[nt][1]);
@@ -599,8 +638,8 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
             for (int m = 0; m < MTW; ++m) {
               const int mtg = (D == 128) ? m : (warp & 1);
               uint32_t a0, a1, a2, a3;
-              a_pairs_2bit(W0, mtg, a0, a1);
-              a_pairs_2bit(W1, mtg, a2, a3);
+              a_pairs_2bit<true>(W0, mtg, a0, a1);
+              a_pairs_2bit<true>(W1, mtg, a2, a3);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 if (nt != nt_ri) continue;
@@ -618,8 +657,8 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
             for (int m = 0; m < MTW; ++m) {
               const int mtg = (D == 128) ? m : (warp & 1);
               uint32_t a0, a1, a2, a3;
-              a_pairs_4bit(W0, mtg, a0, a1);
-              a_pairs_4bit(W1, mtg, a2, a3);
+              a_pairs_4bit<true>(W0, mtg, a0, a1);
+              a_pairs_4bit<true>(W1, mtg, a2, a3);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 if (nt != nt_ri) continue;
@@ -701,7 +740,7 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {      // hh: row r (j even) or row r+8 (j odd)
           const int j = 2 * mtg + hh;
-          const float sc4 = (j & 1) ? 0.0625f : 1.f;
+          const float sc4 = (j & 1) ? 0.0625f : 1.f;      // value codes are normal fp16
           const float sc2 = 1.f / float(1 << (2 * j));
           const float vr = accR[m][nt][2 * hh + e] * sc4 + oR;
           float ve = accE2[m][nt][2 * hh + e] * sc2 + oE;
@@ -717,14 +756,32 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
 using KernelFn = void (*)(MmaArgs);
 
 template <int D>
-KernelFn pick_kernel(int nt, bool res4) {
-  if (nt == 1) return res4 ? rq_mma_kernel<D, 1, true> : rq_mma_kernel<D, 1, false>;
-  if (nt == 2) return res4 ? rq_mma_kernel<D, 2, true> : rq_mma_kernel<D, 2, false>;
-  return res4 ? rq_mma_kernel<D, 4, true> : rq_mma_kernel<D, 4, false>;
+KernelFn pick_generic(int nt, bool res4) {
+  if (nt == 1) return res4 ? rq_mma_kernel<D, 1, true, -1> : rq_mma_kernel<D, 1, false, -1>;
+  if (nt == 2) return res4 ? rq_mma_kernel<D, 2, true, -1> : rq_mma_kernel<D, 2, false, -1>;
+  return res4 ? rq_mma_kernel<D, 4, true, -1> : rq_mma_kernel<D, 4, false, -1>;
 }
 
-KernelFn pick(int D, int nt, bool res4) {
-  return D == 128 ? pick_kernel<128>(nt, res4) : pick_kernel<64>(nt, res4);
+// Variants with the residual-loop count fixed at compile time, for the common blocks: one
+// loop of a per-loop call (0 or 1 residual), all four loops of a 4-loop model (3) and all
+// eight loops of an 8-loop model (7).
+KernelFn pick(int D, int nt, bool res4, int nr) {
+  if (D == 128 && nt == 1 && !res4) {
+    if (nr == 0) return rq_mma_kernel<128, 1, false, 0>;
+    if (nr == 1) return rq_mma_kernel<128, 1, false, 1>;
+    if (nr == 3) return rq_mma_kernel<128, 1, false, 3>;
+  }
+  if (D == 128 && nt == 1 && res4) {
+    if (nr == 1) return rq_mma_kernel<128, 1, true, 1>;
+    if (nr == 3) return rq_mma_kernel<128, 1, true, 3>;
+  }
+  if (D == 128 && nt == 4 && !res4 && nr == 7) return rq_mma_kernel<128, 4, false, 7>;
+  if (D == 64 && nt == 1 && !res4) {
+    if (nr == 0) return rq_mma_kernel<64, 1, false, 0>;
+    if (nr == 1) return rq_mma_kernel<64, 1, false, 1>;
+    if (nr == 3) return rq_mma_kernel<64, 1, false, 3>;
+  }
+  return D == 128 ? pick_generic<128>(nt, res4) : pick_generic<64>(nt, res4);
 }
 
 // Opt every kernel variant in to the largest dynamic shared memory, once per device.
@@ -737,21 +794,22 @@ cudaError_t prepare_kernels() {
     err[dev] = cudaSuccess;
     for (int D : {64, 128})
       for (int nt : {1, 2, 4})
-        for (bool r4 : {false, true}) {
-          cudaError_t e = cudaFuncSetAttribute(pick(D, nt, r4),
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               200 * 1024);
-          if (e != cudaSuccess) err[dev] = e;
-        }
+        for (bool r4 : {false, true})
+          for (int nr = -1; nr <= kMaxResPerBlock; ++nr) {
+            cudaError_t e = cudaFuncSetAttribute(pick(D, nt, r4, nr),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 200 * 1024);
+            if (e != cudaSuccess) err[dev] = e;
+          }
   });
   return err[dev];
 }
 
 // CTAs of a kernel variant resident per SM with `smem` bytes of dynamic shared memory.
-int resident_ctas(int D, int nt, bool res4, size_t smem) {
+int resident_ctas(int D, int nt, bool res4, int nr, size_t smem) {
   int n = 0;
   if (prepare_kernels() == cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, nt, res4), kW * 32, smem) ==
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, nt, res4, nr), kW * 32, smem) ==
           cudaSuccess &&
       n > 0)
     return n;
@@ -809,7 +867,7 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
   for (int stages = 3; stages >= 2; --stages) {
     const size_t sm = smem_layout(D, bl.nt, res4, stages, a.stage_bytes).total;
     if (sm > 200 * 1024) continue;
-    const int ctas = resident_ctas(D, bl.nt, res4, sm);
+    const int ctas = resident_ctas(D, bl.nt, res4, bq.nr, sm);
     if (ctas > best_ctas) {
       best_ctas = ctas;
       a.n_stages = stages;
@@ -863,7 +921,7 @@ SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int 
   for (int i = 0; i < nb; ++i) {
     BlockLaunch bl;
     if (!build_block(s, dummy, blocks[i], bl)) continue;
-    const int n = resident_ctas(s.head_dim, bl.nt, bl.res4, bl.smem);
+    const int n = resident_ctas(s.head_dim, bl.nt, bl.res4, blocks[i].nr, bl.smem);
     if (ctas == 0 || n < ctas) ctas = n;
   }
   return plan_splits_for(s, max_ctx, ctas > 0 ? ctas : 1, kT);
@@ -901,7 +959,7 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.tokens_per_split = tokens_per_split;
     a.scale_log2 = scale * kLog2e;
     dim3 grid(n_splits, s.n_kv_heads, s.batch);
-    pick(s.head_dim, bl.nt, bl.res4)<<<grid, kW * 32, bl.smem, stream>>>(a);
+    pick(s.head_dim, bl.nt, bl.res4, blocks[bi].nr)<<<grid, kW * 32, bl.smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -70,10 +70,16 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two packed codes -> two exact fp16 values: (w & mask) sets the code bits in the low
-// mantissa bits of each 16-bit half; OR-ing 0x6400 makes that half 1024 + value, and one
-// packed subtraction of 1024 leaves the value (code times the power of two of its position).
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t mask) {
+// Two packed codes -> two exact fp16 operands with one AND: code bits masked in place in
+// the low mantissa bits of each 16-bit half (exponent field zero) are the fp16 subnormal
+// (code << k) * 2^-24, k the bit position.  mma.sync takes fp16 subnormal operands exactly on
+// sm_103a (checked by the decode parity tests).
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t mask) { return w & mask; }
+
+// The same pair as exact normal fp16 values: OR-ing 0x6400 makes each half 1024 + value and
+// one packed subtraction of 1024 leaves the value (code times the power of two of its bit
+// position).  Used where the other operand may itself be subnormal.
+__device__ __forceinline__ uint32_t code_pair_normal(uint32_t w, uint32_t mask) {
   uint32_t t;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(w), "r"(mask), "r"(0x64006400u));
   uint32_t out;
