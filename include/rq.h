@@ -147,6 +147,27 @@ rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k,
                                    const int32_t* ctx_lens, int32_t max_ctx, uint16_t* out,
                                    void* ws, size_t ws_bytes, void* stream);
 
+/* Decode attention without a caller-provided workspace, for callers that cannot allocate
+ * device memory: e.g. a plug-in whose host framework owns every device allocation and hands
+ * it only input and output tensors, or a C caller that must not allocate once it has
+ * started.  (The method's pages have no counterpart: this is an interface choice.)
+ * The split-KV scratch lives in a fixed device array of rq_decode_noalloc_scratch_bytes()
+ * bytes (32 MiB) inside the library; every GPU that loads the library holds that array until
+ * the process exits.  Arguments are as in rq_decode_attention without ws / ws_bytes.
+ *   - A call whose scratch need (rq_decode_workspace_bytes) exceeds the array returns
+ *     RQ_ERR_WORKSPACE and enqueues nothing.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - No allocation of any kind: no cudaMalloc, cudaFree or allocating library routine.
+ *   - All calls share the one array and it keeps the last call's contents: calls whose
+ *     executions overlap on the GPU (other streams, other host threads) race on it, so
+ *     serialise them.  Each call clears what must start at zero itself. */
+size_t rq_decode_noalloc_scratch_bytes(void);
+rq_status rq_decode_attention_noalloc(const rq_shape* shape, const rq_cache* cache,
+                                      const uint16_t* q, int32_t loop_begin, int32_t loop_count,
+                                      const uint16_t* pending_kv, const int32_t* ctx_lens,
+                                      int32_t max_ctx, uint16_t* out, void* stream);
+
 /* Human-readable name of a status. */
 const char* rq_status_str(rq_status status);
 

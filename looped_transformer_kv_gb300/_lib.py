@@ -14,7 +14,8 @@ STATUS = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_UNSUPPORTED",
 
 EXPORTS = ("rq_cache_bytes", "rq_encode_append", "rq_decode_workspace_bytes",
            "rq_decode_attention", "rq_bf16_decode_attention", "rq_status_str",
-           "rq_synth_states", "rq_synth_queries")
+           "rq_synth_states", "rq_synth_queries", "rq_decode_noalloc_scratch_bytes",
+           "rq_decode_attention_noalloc")
 
 
 class RqShape(ctypes.Structure):
@@ -72,6 +73,10 @@ def lib():
     L.rq_decode_attention.restype = i32
     L.rq_bf16_decode_attention.argtypes = [S, _P, _P, _P, i32, i32, _P, _P, i32, _P, _P, sz, _P]
     L.rq_bf16_decode_attention.restype = i32
+    L.rq_decode_noalloc_scratch_bytes.argtypes = []
+    L.rq_decode_noalloc_scratch_bytes.restype = sz
+    L.rq_decode_attention_noalloc.argtypes = [S, C, _P, i32, i32, _P, _P, i32, _P, _P]
+    L.rq_decode_attention_noalloc.restype = i32
     L.rq_status_str.argtypes = [i32]
     L.rq_status_str.restype = ctypes.c_char_p
     P = ctypes.POINTER(RqSynthParams)

@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["rq_api.cu", "rq_encode.cu", "rq_decode.cu", "rq_decode_mma.cu", "rq_bf16.cu",
-           "rq_synth.cu"]
+           "rq_synth.cu", "rq_noalloc.cu"]
 
 
 def nvcc():

@@ -1,0 +1,57 @@
+// rq_decode_attention_noalloc: decode attention for callers that cannot allocate device
+// memory.  The split-KV scratch (error word + partial records) lives in one file-scope
+// device array instead of a caller-provided workspace.
+#include <mutex>
+
+#include "rq_common.cuh"
+#include "rq_kernels.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB, fixed at build time
+
+// Held by every GPU that loads the library, from load until process exit.
+static __device__ __align__(256) unsigned char g_rq_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_once[kMaxDevices];
+void* g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+
+// Device address of the scratch array on the current device.  In host code the array's
+// name is only a host-side stand-in, so the address is looked up once per device, with
+// that device current, and kept.
+rq_status scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RQ_ERR_CUDA;
+  std::call_once(g_once[dev], [dev] {
+    void* p = nullptr;
+    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_rq_scratch);
+    g_scratch_ptr[dev] = p;
+  });
+  if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return RQ_ERR_CUDA;
+  *out = g_scratch_ptr[dev];
+  return RQ_OK;
+}
+
+}  // namespace
+
+extern "C" size_t rq_decode_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" rq_status rq_decode_attention_noalloc(const rq_shape* shape, const rq_cache* cache,
+                                                 const uint16_t* q, int32_t loop_begin,
+                                                 int32_t loop_count, const uint16_t* pending_kv,
+                                                 const int32_t* ctx_lens, int32_t max_ctx,
+                                                 uint16_t* out, void* stream) {
+  if (!shape) return RQ_ERR_INVALID_ARG;
+  const size_t need = rq_decode_workspace_bytes(shape, loop_count, max_ctx);
+  if (need == 0) return RQ_ERR_INVALID_ARG;          // invalid shape or loop range
+  if (need > kNoAllocScratchBytes) return RQ_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const rq_status st = scratch_for_current_device(&ws);
+  if (st != RQ_OK) return st;
+  // the scratch array's error word is cleared by the call itself; every partial record the
+  // combine reads is rewritten by the split kernel, so nothing else needs clearing
+  return rq_decode_attention(shape, cache, q, loop_begin, loop_count, pending_kv, ctx_lens,
+                             max_ctx, out, ws, kNoAllocScratchBytes, stream);
+}

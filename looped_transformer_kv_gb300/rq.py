@@ -107,6 +107,19 @@ def decode_attention(shape, cache, q, loop_begin, loop_count, pending_kv, ctx_le
         ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def decode_attention_noalloc(shape, cache, q, loop_begin, loop_count, pending_kv, ctx_lens,
+                             max_ctx, out, stream=None):
+    """rq_decode_attention_noalloc: the library's fixed scratch array instead of a workspace."""
+    check("rq_decode_attention_noalloc", _lib.lib().rq_decode_attention_noalloc(
+        ctypes.byref(shape), ctypes.byref(cache.struct), _ptr(q), int(loop_begin),
+        int(loop_count), _ptr(pending_kv), _ptr(ctx_lens), int(max_ctx), _ptr(out),
+        _stream(stream)))
+
+
+def noalloc_scratch_bytes():
+    return int(_lib.lib().rq_decode_noalloc_scratch_bytes())
+
+
 def bf16_decode_attention(shape, k, v, q, loop_begin, loop_count, pending_kv, ctx_lens, max_ctx,
                           out, ws, stream=None):
     check("rq_bf16_decode_attention", _lib.lib().rq_bf16_decode_attention(
