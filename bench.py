@@ -27,6 +27,42 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn KV tokens/s at 1 GB300, HBM GB/s vs peak, vs in-build BF16 kernel"
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one all-loops decode launch
+# of the split kernel, from one ncu capture (profiles/), keyed by the kernel sources they
+# were taken on; any change to those sources makes the figure stale (reported as null).
+KERNEL_SOURCES = ("looped_transformer_kv_gb300/csrc/rq_decode_mma.cu",
+                  "looped_transformer_kv_gb300/csrc/rq_ptx.cuh",
+                  "looped_transformer_kv_gb300/csrc/rq_common.cuh",
+                  "looped_transformer_kv_gb300/csrc/rq_kernels.h")
+TRAFFIC = {
+    ("e30902e80e37a98e", "layer_1p4b"): 482835968 + 7121664,   # profiles/rq_mma_kernel_layer_1p4b.md
+}
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload):
+    t = TRAFFIC.get((_kernel_hash(), workload))
+    return t
+
+
+def reduce_step_ms(ms, world):
+    """Max of the per-rank step times over all ranks (every rank gets the max)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
 
 def _peaks():
     try:
@@ -117,7 +153,7 @@ def _workload_desc(cfg):
     return ("%s: B %d, Hq %d / Hkv %d, d %d, %d loops (INT4 ref, residual bits %s), ctx %d, "
             "group 32, layers %d" % (cfg.name, cfg.batch, cfg.n_q_heads, cfg.n_kv_heads,
                                      cfg.head_dim, cfg.n_loops,
-                                     "/".join(str(b) for b in cfg.res_bits), cfg.ctx, 1))
+                                     "/".join(str(b) for b in cfg.res_bits), cfg.ctx, cfg.layers))
 
 
 class Clocks:
@@ -190,9 +226,14 @@ def gpu_arm(args, cfg):
                          (min(4, cfg.n_kv_heads) - 1, cfg.ctx, cfg.n_loops, len(times),
                           sum(times))}
 
-    # two spare slots past ctx: the deferred write of the current token lands in slot ctx,
-    # which the step's attention (ctx_lens = ctx) does not read, so every step is the same
-    w = Workload(cfg, capacity=cfg.ctx + 2, build_bf16=not args.no_bf16)
+    # spare slots past ctx: the deferred write of the current token lands in slot ctx,
+    # which the step's attention (ctx_lens = ctx) does not read, so every step is the same.
+    # Every layer of the model gets its own packed cache (the BF16 cache of one layer is
+    # built for the comparison kernel: the same shapes for every layer).
+    layers = [Workload(cfg, layer=l, capacity=cfg.ctx + 2, build_bf16=(l == 0 and not args.no_bf16))
+              for l in range(cfg.layers)]
+    w = layers[0]
+    NL = len(layers)
     L, B, ctx = cfg.n_loops, w.B, cfg.ctx
     stream = torch.cuda.current_stream()
     out = w.out_buffer(L)
@@ -203,12 +244,16 @@ def gpu_arm(args, cfg):
     new_kv = w.pending.reshape(B, 1, 2, L, w.H, w.d)
     pos_new = torch.full((B, 1), ctx, dtype=torch.int32, device="cuda")
 
+    outs = [out] + [lw.out_buffer(L) for lw in layers[1:]]
+
     def step():
-        w.decode(0, L, out, ws)
-        rqm.encode_append(w.shape, w.cache, new_kv, positions=pos_new)
+        for lw, o in zip(layers, outs):
+            lw.decode(0, L, o, ws)
+            rqm.encode_append(lw.shape, lw.cache, lw.pending.reshape(B, 1, 2, L, w.H, w.d),
+                              positions=pos_new)
 
     g = w.Hq // w.H
-    launches_per_step = math.ceil(g * L / 8) + 1 + 1
+    launches_per_step = NL * (math.ceil(g * L / 8) + 1 + 1)
 
     def graph_of(fn):
         """Capture fn (a sequence of library calls on the current stream) in a CUDA graph."""
@@ -252,10 +297,8 @@ def gpu_arm(args, cfg):
     stop.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop) / args.steps
+    ms = reduce_step_ms(ms, world)
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
 
     # ---- per-call timings (graph replays, same stream, CUDA events) ----
@@ -281,15 +324,19 @@ def gpu_arm(args, cfg):
     clk = clocks.stop()
 
     # ---- end to end through the public API with host buffers ----
-    q_h = w.q.cpu().pin_memory()
-    p_h = w.pending.cpu().pin_memory()
-    o_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    # every step: the layers' queries and current-token states from pinned host memory,
+    # and the layers' outputs back
+    q_h = [lw.q.cpu().pin_memory() for lw in layers]
+    p_h = [lw.pending.cpu().pin_memory() for lw in layers]
+    o_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
 
     def e2e_step():
-        w.q.copy_(q_h, non_blocking=True)
-        w.pending.copy_(p_h, non_blocking=True)
+        for lw, qh, ph in zip(layers, q_h, p_h):
+            lw.q.copy_(qh, non_blocking=True)
+            lw.pending.copy_(ph, non_blocking=True)
         step()
-        o_h.copy_(out, non_blocking=True)
+        for oh, o in zip(o_h, outs):
+            oh.copy_(o, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -301,19 +348,19 @@ def gpu_arm(args, cfg):
     ev1.record(stream)
     torch.cuda.synchronize()
     t_e2e = ev0.elapsed_time(ev1) / args.steps
-    h2d = q_h.numel() * 2 + p_h.numel() * 2
-    d2h = o_h.numel() * 2
+    h2d = sum(x.numel() * 2 for x in q_h + p_h)
+    d2h = sum(x.numel() * 2 for x in o_h)
 
     # ---- bytes ----
     d, ng = cfg.head_dim, cfg.head_dim // 32
     ref_b = 2 * (d // 2 + 4 * ng)
     res_b = [2 * (d * b // 8 + 4 * ng + 2) for b in cfg.res_bits[: L - 1]]
-    th = B * w.H * ctx
+    th = B * w.H * ctx                                   # token-heads of one layer
     io_b = w.q.numel() * 2 + w.pending.numel() * 2 + out.numel() * 2
     bytes_multi = th * (ref_b + sum(res_b)) + io_b
     bytes_per = th * (L * ref_b + sum(res_b)) + io_b
     bytes_bf16 = th * L * 2 * d * 2 + io_b
-    kvtok = B * ctx * L
+    kvtok = B * ctx * L                                  # per layer
     hbm, peak_kind = _peaks()
 
     def med(x):
@@ -340,7 +387,7 @@ def gpu_arm(args, cfg):
                                         "perloop": med(t_bf_per) / med(t_per)}
     breakdown["storage_reduction_vs_bf16"] = 1 - (ref_b + sum(res_b)) / (L * 2 * d * 2)
 
-    value = kvtok * world / (ms * 1e-3)
+    value = kvtok * NL * world / (ms * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -348,15 +395,15 @@ def gpu_arm(args, cfg):
         "data": "synthetic (seeded Philox generator; no dataset)",
         "config": {"workload": _workload_desc(cfg), "step": "multi-loop decode attention + "
                    "deferred-write encode/append of the current token (CUDA graph replay)",
-                   "layers_timed": 1,
+                   "layers_timed": NL,
                    "l2": "inputs larger than L2 (%.0f MB packed cache read per step)" %
                    (bytes_multi / 1e6), "parallelism": "replicas (weak, per-GPU batch %d)" % B},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "traffic": None, "peak_kind": peak_kind,
+                     "frac": gbs / hbm, "traffic": _traffic(cfg.name), "peak_kind": peak_kind,
                      "kernel": "rq_decode_attention (split kernel + combine, timed per call)",
                      "algorithmic_bytes_per_launch": bytes_multi},
         "cpu_baseline": cpu,
-        "e2e": {"value": kvtok * world / (t_e2e * 1e-3), "unit": "KV tokens/s",
+        "e2e": {"value": kvtok * NL * world / (t_e2e * 1e-3), "unit": "KV tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
