@@ -756,32 +756,31 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
 using KernelFn = void (*)(MmaArgs);
 
 template <int D>
-KernelFn pick_generic(int nt, bool res4) {
-  if (nt == 1) return res4 ? rq_mma_kernel<D, 1, true, -1> : rq_mma_kernel<D, 1, false, -1>;
-  if (nt == 2) return res4 ? rq_mma_kernel<D, 2, true, -1> : rq_mma_kernel<D, 2, false, -1>;
-  return res4 ? rq_mma_kernel<D, 4, true, -1> : rq_mma_kernel<D, 4, false, -1>;
+KernelFn pick_generic(bool res4) {
+  return res4 ? rq_mma_kernel<D, 1, true, -1> : rq_mma_kernel<D, 1, false, -1>;
 }
 
 // Variants with the residual-loop count fixed at compile time, for the common blocks: one
-// loop of a per-loop call (0 or 1 residual), all four loops of a 4-loop model (3) and all
-// eight loops of an 8-loop model (7).
+// loop of a per-loop call (0 or 1 residual), two loops of a 4-query-head GQA block (2) and
+// all four loops of a 4-loop model (3).
 KernelFn pick(int D, int nt, bool res4, int nr) {
   if (D == 128 && nt == 1 && !res4) {
     if (nr == 0) return rq_mma_kernel<128, 1, false, 0>;
     if (nr == 1) return rq_mma_kernel<128, 1, false, 1>;
+    if (nr == 2) return rq_mma_kernel<128, 1, false, 2>;
     if (nr == 3) return rq_mma_kernel<128, 1, false, 3>;
   }
   if (D == 128 && nt == 1 && res4) {
     if (nr == 1) return rq_mma_kernel<128, 1, true, 1>;
     if (nr == 3) return rq_mma_kernel<128, 1, true, 3>;
   }
-  if (D == 128 && nt == 4 && !res4 && nr == 7) return rq_mma_kernel<128, 4, false, 7>;
   if (D == 64 && nt == 1 && !res4) {
     if (nr == 0) return rq_mma_kernel<64, 1, false, 0>;
     if (nr == 1) return rq_mma_kernel<64, 1, false, 1>;
     if (nr == 3) return rq_mma_kernel<64, 1, false, 3>;
   }
-  return D == 128 ? pick_generic<128>(nt, res4) : pick_generic<64>(nt, res4);
+  (void)nt;                                     // blocks hold one n-tile (8 columns)
+  return D == 128 ? pick_generic<128>(res4) : pick_generic<64>(res4);
 }
 
 // Opt every kernel variant in to the largest dynamic shared memory, once per device.
@@ -793,7 +792,7 @@ cudaError_t prepare_kernels() {
   std::call_once(once[dev], [&] {
     err[dev] = cudaSuccess;
     for (int D : {64, 128})
-      for (int nt : {1, 2, 4})
+      for (int nt : {1})
         for (bool r4 : {false, true})
           for (int nr = -1; nr <= kMaxResPerBlock; ++nr) {
             cudaError_t e = cudaFuncSetAttribute(pick(D, nt, r4, nr),
@@ -880,6 +879,11 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
 
 }  // namespace
 
+// Query columns per launch: one 8-column n-tile keeps registers and shared memory low enough
+// for three resident CTAs per SM; wider blocks (which read the reference tile once for more
+// loops) measured slower on GB300 because of the lower occupancy.
+constexpr int kMaxBlockColumns = 8;
+
 int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* out, int max_out) {
   int gw = 1;
   while (gw < g && gw < 8) gw <<= 1;
@@ -893,7 +897,7 @@ int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* 
       bq.gw = gw;
       bq.lb = l;
       int nl = 0, nres = 0;
-      while (l + nl < lend && (nl + 1) * gw <= 32) {
+      while (l + nl < lend && (nl + 1) * gw <= kMaxBlockColumns) {
         const bool res = (l + nl) != L - 1;
         if (res && nres == kMaxResPerBlock) break;
         nres += res;
