@@ -1,25 +1,37 @@
 // ResidualQuant split-KV decode attention on the tensor cores (sm_103a).
 //
-// Per CTA: one (split of the context, kv-head, sequence); 4 warps; 64-token tiles of every
-// packed array are staged in shared memory by 1-D bulk (TMA) copies through a multi-stage
-// mbarrier pipeline.  For a loop-l query q and token t (rit.work summary, "How each pass's
-// KV cache is reconstructed": reference and residuals rebuilt inside attention)
+// Per CTA: one (split of the context, kv-head, sequence) and one block of at most 8 query
+// columns; 4 warps; 64-token tiles of every packed array are staged in shared memory by 1-D
+// bulk (TMA) copies through a multi-stage mbarrier pipeline.  For a loop-l query q and token
+// t (rit.work summary, "How each pass's KV cache is reconstructed": reference and residuals
+// rebuilt inside attention)
 //   score_t = a_t * sum_g [s^r_g,t (q_g . c^r_g,t) + z^r_g,t sum(q_g)]
 //           +       sum_g [s^e_g,t (q'_g . c^e_g,t) + z^e_g,t sum(q'_g)],      q' = R q
 //   acc_ref += p_t a_t (s^r c^r + z^r),   acc_res += p_t (s^e c^e + z^e)   (rotated domain)
-// The code dot products and the P.V products run as mma.sync m16n8k16 (f16 in, f32 acc):
-//   scores: M = 16 tokens, N = 8 query columns, K = 16 channels of one 32-channel group;
-//   values: M = 16 channels of one group, N = 8 query columns, K = 16 tokens.
-// A pair of packed codes becomes an f16x2 operand with one AND: the code bits, masked in
-// place with a zero exponent field, are the fp16 subnormal c * 2^-24 times a power of two
-// fixed by their bit position; that power is folded into the query fragments (scores) or
-// removed per output row at the end (values), and 2^24 is restored in fp32.  The other operand (queries, softmax weights) is split into an fp16 high part
-// and an fp16 low part (two MMAs) and so carries about 22 significant bits; products are
-// exact in the fp32 accumulators.
-// Query columns of every loop share the fragments: the residual codes of loop l meet a
-// query fragment whose columns of other loops are masked to zero, so all residual loops
-// accumulate into one score fragment per group (scaled once by each column's own step and
-// offset) and into one value accumulator per residual bit width.
+//
+// Each warp owns 16 tokens of every tile from scores to values, with its own online-softmax
+// state, so no warp waits for another inside the loop:
+//   scores: mma.sync m16n8k16, M = the warp's 16 tokens, N = 8 query columns, K = 16
+//           channels; A = packed K codes, B = query fragments;
+//   softmax: warp-local running max per column (raised lazily, only when a tile's maximum
+//           exceeds it by more than 2^4 in probability), exponentials in the score fragment;
+//   values: M = 16 channels, N = 8 columns, K = the warp's 16 tokens; A = packed V codes,
+//           B = softmax weights p * a * step, moved from the score fragment's layout to the
+//           B-operand layout in registers by movmatrix transposes.
+// A stage is refilled by the last warp to finish with it; the four warps' partial results
+// are merged once per CTA at the end.
+//
+// A pair of packed codes becomes an f16x2 operand with one AND (scores: the masked bits are
+// the fp16 subnormal c * 2^-24 times a power of two fixed by their bit position, folded into
+// the query fragments, with 2^24 restored in fp32) or with an OR and a packed subtraction
+// (values: exact normal fp16 code times a power of two removed per output row at the end).
+// The other operand (queries, softmax weights) is split into an fp16 high part and an fp16
+// low part (two MMAs) and so carries about 22 significant bits; products are exact in the
+// fp32 accumulators.
+// Query columns of every loop share the fragments: the residual codes of loop l meet the
+// query fragments of every column, and each column keeps only its own loop's dot product
+// (a per-loop score accumulator, or a query fragment masked to the loop's columns); in the
+// value phase the weights of loop l's residual codes are masked to loop l's columns.
 #include <mutex>
 
 #include "rq_common.cuh"
@@ -30,7 +42,10 @@ namespace rq {
 namespace {
 
 constexpr int kT = 64;                        // tokens per tile
-constexpr int kW = 4;                         // warps per CTA
+constexpr int kW = 4;                         // warps per CTA; warp w owns tokens [16w, 16w+16)
+constexpr int kNQ = 8;                        // query columns of a block (one n-tile)
+constexpr float kRescaleSlack = 4.f;          // log2 units: weights stay <= 2^4 between rescales
+constexpr int kIssuedSlot = 15;               // release-counter word holding the tiles issued
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct MmaArgs {
@@ -82,6 +97,10 @@ __device__ __forceinline__ float2 ld_meta(const uint8_t* p) {  // (step, offset)
   return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
 
+__device__ __forceinline__ float2 meta_f2(uint32_t w) {  // packed (step, offset) -> fp32
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
 __device__ __forceinline__ float ld_half(const uint8_t* p) {
   return __half2float(*reinterpret_cast<const __half*>(p));
 }
@@ -94,8 +113,35 @@ __device__ __forceinline__ int pick_int(const int (&arr)[kMaxResPerBlock], int i
   return v;
 }
 
+// m ? x : y for a mask m of all ones or all zeros, as bit operations (one LOP3)
+__device__ __forceinline__ float blend(uint32_t m, float x, float y) {
+  return __uint_as_float((__float_as_uint(x) & m) | (__float_as_uint(y) & ~m));
+}
+
 __device__ __forceinline__ uint4 sel4(bool keep, uint4 v) {
   return keep ? v : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held one row-pair per lane (lane 4i + j holds
+// row i, columns 2j and 2j+1): afterwards the lane holds row i, columns 2j, 2j+1 of the
+// transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_u32(p)), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 4-bit group row (16 bytes) of one token: the A-operand pairs of k-step s for this lane's
@@ -118,15 +164,31 @@ __device__ __forceinline__ void a_pairs_2bit(uint32_t x, int s, uint32_t& lo, ui
   hi = NORMAL ? code_pair_normal(x, m1) : code_pair(x, m1);
 }
 
+// Softmax weights of one channel group in the score-fragment layout (token rows tr0 = r and
+// tr1 = r + 8 of the warp, columns 2c and 2c + 1) -> the B-operand pairs of the value MMA
+// (tokens 2c, 2c+1 | 2c+8, 2c+9 of the warp, column r), split into fp16 high and low parts.
+__device__ __forceinline__ void weights_to_b(float w00, float w01, float w10, float w11,
+                                             uint32_t& bh0, uint32_t& bh1, uint32_t& bl0,
+                                             uint32_t& bl1) {
+  uint32_t hT, lT, hB, lB;
+  split_half2(w00, w01, hT, lT);
+  split_half2(w10, w11, hB, lB);
+  bh0 = movmatrix_trans(hT);
+  bh1 = movmatrix_trans(hB);
+  bl0 = movmatrix_trans(lT);
+  bl1 = movmatrix_trans(lB);
+}
+
 // NRT >= 0: the block's number of residual loops, fixed at compile time; -1: read at run time.
-template <int D, int NT, bool RES4, int NRT>
-__global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
+template <int D, bool RES4, int NRT>
+__global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NG = D / 32;
-  constexpr int NQP = NT * 8;        // query columns (padded)
+  constexpr int NQ = kNQ;
   constexpr int P = D / 32;          // channels per lane in the query prep
   constexpr int RB4 = D / 2;         // bytes of a 4-bit row
   constexpr int RB2 = D / 4;         // bytes of a 2-bit row
-  constexpr int MTW = (D == 128) ? 2 : 1;  // 16-channel M-tiles per warp in the value phase
+  constexpr int MT = D / 16;         // 16-channel m-tiles of the value phase (2 per group)
+  constexpr bool PER_LOOP = NRT >= 1 && NRT <= 3;   // one residual score accumulator per loop
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,17 +197,14 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
   const QueryBlock blk = a.blk;
   const int nr = NRT >= 0 ? NRT : blk.nr;
 
-  const SmemLayout lay = smem_layout(D, NT, RES4, a.n_stages, a.stage_bytes);
-  const int PR = lay.prow;
+  const SmemLayout lay = smem_layout(D, RES4, a.n_stages, a.stage_bytes);
   uint4* QF = reinterpret_cast<uint4*>(smem + lay.qf);
   uint4* QR2 = reinterpret_cast<uint4*>(smem + lay.qr2);
   uint4* QR4 = reinterpret_cast<uint4*>(smem + lay.qr4);
   float* Qsum = reinterpret_cast<float*>(smem + lay.qsum);
   float* QRsum = reinterpret_cast<float*>(smem + lay.qrsum);
-  float* Ps = reinterpret_cast<float*>(smem + lay.ps);
-  float* Pa = reinterpret_cast<float*>(smem + lay.pa);
-  float* red = reinterpret_cast<float*>(smem + lay.red);
-  float* mrun = reinterpret_cast<float*>(smem + lay.mrun);
+  float* red = reinterpret_cast<float*>(smem + lay.red);      // [2][kW][NQ]
+  unsigned* cnt = reinterpret_cast<unsigned*>(smem + lay.cnt);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
 
   // residual index (into the block's residual loops) of query column n, -1 if the column
@@ -156,12 +215,55 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
     return (li < blk.nl && gi < a.g && l != a.L - 1) ? l - blk.r0 : -1;
   };
 
+  // ------------------------------------------------------------------ pipeline set-up
+  // (first: the first tiles stream in while the queries are prepared)
+  const int ctx = min(a.ctx_lens[b], a.cap);
+  const int t_begin = split * a.tokens_per_split;
+  const int t_end = min(ctx, t_begin + a.tokens_per_split);
+  const int ntiles = t_end > t_begin ? (t_end - t_begin + kT - 1) / kT : 0;
+  const int64_t slot = int64_t(b) * a.H + h;
+  const int S = a.n_stages;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);
+      cnt[s] = 0u;
+    }
+    fence_mbar_init();
+  }
+
+  auto issue = [&](int tile) {
+    const int st = tile % S;
+    const uint32_t bar = smem_u32(&bars[st]);
+    const uint32_t dst = smem_u32(smem + st * a.stage_bytes);
+    const int64_t tok = slot * a.cap + t_begin + int64_t(tile) * kT;
+    mbar_arrive_expect_tx(bar, uint32_t(a.stage_bytes));
+    bulk_g2s(dst + a.off_kc, a.kc + tok * RB4, kT * RB4, bar);
+    bulk_g2s(dst + a.off_km, a.km + tok * NG * 2, kT * NG * 4, bar);
+    bulk_g2s(dst + a.off_vc, a.vc + tok * RB4, kT * RB4, bar);
+    bulk_g2s(dst + a.off_vm, a.vm + tok * NG * 2, kT * NG * 4, bar);
+#pragma unroll
+    for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
+      if (ri >= nr) break;
+      const int rb = (!RES4 || a.rbits[ri] == 2) ? RB2 : RB4;
+      bulk_g2s(dst + a.off_krc[ri], a.krc[ri] + tok * rb, kT * rb, bar);
+      bulk_g2s(dst + a.off_krm[ri], a.krm[ri] + tok * NG * 2, kT * NG * 4, bar);
+      bulk_g2s(dst + a.off_ka[ri], a.ka[ri] + tok, kT * 2, bar);
+      bulk_g2s(dst + a.off_vrc[ri], a.vrc[ri] + tok * rb, kT * rb, bar);
+      bulk_g2s(dst + a.off_vrm[ri], a.vrm[ri] + tok * NG * 2, kT * NG * 4, bar);
+      bulk_g2s(dst + a.off_va[ri], a.va[ri] + tok, kT * 2, bar);
+    }
+  };
+  if (threadIdx.x == 0) {   // the barriers' initialisation is ordered before by the fence
+    const int n0 = S < ntiles ? S : ntiles;
+    for (int i = 0; i < n0; ++i) issue(i);
+    cnt[kIssuedSlot] = unsigned(n0);
+  }
+
   // ------------------------------------------------------------------ query preparation
   {
     uint32_t* z32 = reinterpret_cast<uint32_t*>(smem + lay.qf);
-    const int nz = (lay.mrun - lay.qf) / 4;
+    const int nz = (lay.cnt - lay.qf) / 4;
     for (int i = threadIdx.x; i < nz; i += blockDim.x) z32[i] = 0u;
-    for (int i = threadIdx.x; i < NQP; i += blockDim.x) mrun[i] = -INFINITY;
   }
   __syncthreads();
   // query columns of this block: scaled q, rotated q' = R q, per-group sums
@@ -194,7 +296,7 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
   // subnormal code operands of the score MMAs)
   {
     float mx = 0.f;
-    for (int n = warp; n < NQP; n += kW) {
+    for (int n = warp; n < NQ; n += kW) {
       float v[P], rr[P];
       prep_column(n, v, rr);
 #pragma unroll
@@ -213,13 +315,12 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
   }
   const float qscale = ldexpf(1.f, qexp);
   const float code_unit = ldexpf(1.f, 24 - qexp);   // undoes 2^-24 codes and the q scale
-  __syncthreads();
-  if (threadIdx.x == 0) *reinterpret_cast<unsigned*>(red) = 0u;
-  // pass 2: fragments and group sums
-  for (int n = warp; n < NQP; n += kW) {
+  const float inv_code_unit = ldexpf(1.f, qexp - 24);
+  // pass 2: fragments and group sums (the sums in units of code_unit, which scales the score
+  // once at the end)
+  for (int n = warp; n < NQ; n += kW) {
     float v[P], rr[P];
-    const bool real = prep_column(n, v, rr);
-    (void)real;
+    prep_column(n, v, rr);
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int j = 0; j < P; ++j) {
@@ -235,17 +336,16 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
     const int bits = ri >= 0 ? a.rbits[ri] : 0;
     const int grp = (lane * P) >> 5;
     if ((lane & (32 / P - 1)) == 0) {
-      Qsum[grp * NQP + n] = s1;
-      if (ri >= 0) QRsum[grp * NQP + n] = s2;
+      Qsum[grp * NQ + n] = s1 * inv_code_unit;
+      if (ri >= 0) QRsum[grp * NQ + n] = s2 * inv_code_unit;
     }
-    const int nt = n >> 3, nn = n & 7;
 #pragma unroll
     for (int j = 0; j < P; ++j) {
       const int ch = lane * P + j, gq = ch >> 5, cl = ch & 31;
       const float vq = v[j] * qscale, rq = rr[j] * qscale;
       {  // 4-bit mapping: slot (c4, s, hi, e) <- channel 8 c4 + 2 s + hi + 4 e, scale 16^-hi
         const int c4 = cl >> 3, w8 = cl & 7, s = (w8 >> 1) & 1, hi = w8 & 1, e = w8 >> 2;
-        const int idx = ((gq * 2 + s) * NT + nt) * 32 + nn * 4 + c4;
+        const int idx = (gq * 2 + s) * 32 + n * 4 + c4;
         __half* dq = reinterpret_cast<__half*>(&QF[idx]);
         split_half(hi ? vq * 0.0625f : vq, dq[hi * 2 + e], dq[4 + hi * 2 + e]);
         if (RES4 && bits == 4) {
@@ -257,417 +357,369 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
         const int e = (cl >> 3) & 1, cq = 2 * (cl >> 4) + ((cl & 7) >> 2), jj = cl & 3;
         const int s = jj >> 1, hi = jj & 1;
         const float sc = (jj == 0) ? 1.f : (jj == 1) ? 0.25f : (jj == 2) ? 0.0625f : 0.015625f;
-        __half* dr = reinterpret_cast<__half*>(&QR2[((gq * 2 + s) * NT + nt) * 32 + nn * 4 + cq]);
+        __half* dr = reinterpret_cast<__half*>(&QR2[(gq * 2 + s) * 32 + n * 4 + cq]);
         split_half(rq * sc, dr[hi * 2 + e], dr[4 + hi * 2 + e]);
       }
     }
   }
 
-  // ------------------------------------------------------------------ pipeline set-up
-  const int ctx = min(a.ctx_lens[b], a.cap);
-  const int t_begin = split * a.tokens_per_split;
-  const int t_end = min(ctx, t_begin + a.tokens_per_split);
-  const int ntiles = t_end > t_begin ? (t_end - t_begin + kT - 1) / kT : 0;
-  const int64_t slot = int64_t(b) * a.H + h;
-  const int S = a.n_stages;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bars[s]), 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  auto issue = [&](int tile) {
-    const int st = tile % S;
-    const uint32_t bar = smem_u32(&bars[st]);
-    const uint32_t dst = smem_u32(smem + st * a.stage_bytes);
-    const int64_t tok = slot * a.cap + t_begin + int64_t(tile) * kT;
-    mbar_arrive_expect_tx(bar, uint32_t(a.stage_bytes));
-    bulk_g2s(dst + a.off_kc, a.kc + tok * RB4, kT * RB4, bar);
-    bulk_g2s(dst + a.off_km, a.km + tok * NG * 2, kT * NG * 4, bar);
-    bulk_g2s(dst + a.off_vc, a.vc + tok * RB4, kT * RB4, bar);
-    bulk_g2s(dst + a.off_vm, a.vm + tok * NG * 2, kT * NG * 4, bar);
+  // columns of this lane: score/value-accumulator fragments hold columns 2c and 2c + 1, the
+  // value B operand column r
+  int riD[2], krmD[2], kaD[2], vaD[2], vrmD[2];
 #pragma unroll
-    for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
-      if (ri >= nr) break;
-      const int rb = D * a.rbits[ri] / 8;
-      bulk_g2s(dst + a.off_krc[ri], a.krc[ri] + tok * rb, kT * rb, bar);
-      bulk_g2s(dst + a.off_krm[ri], a.krm[ri] + tok * NG * 2, kT * NG * 4, bar);
-      bulk_g2s(dst + a.off_ka[ri], a.ka[ri] + tok, kT * 2, bar);
-      bulk_g2s(dst + a.off_vrc[ri], a.vrc[ri] + tok * rb, kT * rb, bar);
-      bulk_g2s(dst + a.off_vrm[ri], a.vrm[ri] + tok * NG * 2, kT * NG * 4, bar);
-      bulk_g2s(dst + a.off_va[ri], a.va[ri] + tok, kT * 2, bar);
+  for (int e = 0; e < 2; ++e) {
+    riD[e] = col_ri(2 * c + e);
+    const int rc = riD[e] < 0 ? 0 : riD[e];
+    krmD[e] = pick_int(a.off_krm, rc);
+    kaD[e] = pick_int(a.off_ka, rc);
+    vaD[e] = pick_int(a.off_va, rc);
+    vrmD[e] = pick_int(a.off_vrm, rc);
+  }
+  const int riB = col_ri(r);
+  // loop_mask[e][ri]: all ones where column 2c + e belongs to residual loop ri
+  uint32_t loop_mask[2][PER_LOOP ? NRT : 1];
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int ri = 0; ri < (PER_LOOP ? NRT : 1); ++ri) loop_mask[e][ri] = riD[e] == ri ? ~0u : 0u;
+
+  float accR[MT][4], accE2[MT][4], accE4[RES4 ? MT : 1][4];
+  float offR[NG][2], offE[NG][2];
+  float lsum[2] = {0.f, 0.f}, mw[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      accR[m][k] = 0.f;
+      accE2[m][k] = 0.f;
+      if (RES4) accE4[m][k] = 0.f;
     }
-  };
-  int next_issue = 0;  // tiles issued so far (thread 0)
-  if (threadIdx.x == 0) {
-    for (; next_issue < S && next_issue < ntiles; ++next_issue) issue(next_issue);
-  }
-
-  // residual indices of this lane's B-fragment columns (nt*8 + r) and D-fragment columns
-  // (nt*8 + 2c + e)
-  int riB[NT], riD[NT][2];
-  int krmD[NT][2], kaD[NT][2], vaD[NT][2], vrmB[NT];   // stage offsets of those columns' loops
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    riB[nt] = col_ri(nt * 8 + r);
-    vrmB[nt] = pick_int(a.off_vrm, riB[nt] < 0 ? 0 : riB[nt]);
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      riD[nt][e] = col_ri(nt * 8 + 2 * c + e);
-      const int rc = riD[nt][e] < 0 ? 0 : riD[nt][e];
-      krmD[nt][e] = pick_int(a.off_krm, rc);
-      kaD[nt][e] = pick_int(a.off_ka, rc);
-      vaD[nt][e] = pick_int(a.off_va, rc);
-    }
-  }
-
-  float lpart[NT][2];
-  float accR[MTW][NT][4], accE2[MTW][NT][4], accE4[RES4 ? MTW : 1][NT][4];
-  float offR[NT], offE[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    lpart[nt][0] = lpart[nt][1] = 0.f;
-    offR[nt] = offE[nt] = 0.f;
-#pragma unroll
-    for (int m = 0; m < MTW; ++m)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        accR[m][nt][k] = 0.f;
-        accE2[m][nt][k] = 0.f;
-        if (RES4) accE4[m][nt][k] = 0.f;
-      }
-  }
-  const int gv = (D == 128) ? warp : (warp >> 1);     // value-phase channel group of this warp
+  for (int g = 0; g < NG; ++g) offR[g][0] = offR[g][1] = offE[g][0] = offE[g][1] = 0.f;
 
   bool failed = false;
-  int fail_tile = 0;
+  const int tr0 = 16 * warp + r, tr1 = tr0 + 8;       // this lane's token rows in a tile
+  const int p0 = 8 * warp + c, p1 = p0 + 4;           // token pairs of its value B rows
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % S;
-    const bool ok = mbar_wait_bounded(smem_u32(&bars[st]), uint32_t((i / S) & 1), kWaitLimitNs);
-    const uint8_t* sb = smem + st * a.stage_bytes;
-    const int t0 = t_begin + i * kT;
-
-    // -------------------------------------------------------------- scores (16 tokens/warp)
-    const int tr0 = 16 * warp + r, tr1 = tr0 + 8;
-    const bool v0 = t0 + tr0 < t_end, v1 = t0 + tr1 < t_end;
-    float sc[NT][4];
-    {
-      float Sref[NT][4], Sres[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) Sref[nt][k] = Sres[nt][k] = 0.f;
-      float2 mk0[NG], mk1[NG];
-#pragma unroll
-      for (int gq = 0; gq < NG; ++gq) {
-        mk0[gq] = ld_meta(sb + a.off_km + (tr0 * NG + gq) * 4);
-        mk1[gq] = ld_meta(sb + a.off_km + (tr1 * NG + gq) * 4);
-      }
-      // this lane's word of every group (K rows are group-interleaved: one load)
-      uint32_t kw0[NG], kw1[NG];
-      load_words<NG>(sb + a.off_kc + tr0 * RB4 + c * NG * 4, kw0);
-      load_words<NG>(sb + a.off_kc + tr1 * RB4 + c * NG * 4, kw1);
-#pragma unroll
-      for (int gq = 0; gq < NG; ++gq) {
-        // reference
-        {
-          const uint32_t wl = kw0[gq];
-          const uint32_t wh = kw1[gq];
-          float Dg[NT][4];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) Dg[nt][k] = 0.f;
-#pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            uint32_t a0, a2, a1, a3;
-            a_pairs_4bit(wl, s, a0, a2);
-            a_pairs_4bit(wh, s, a1, a3);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const uint4 bq = QF[((gq * 2 + s) * NT + nt) * 32 + lane];
-              mma_f16(Dg[nt], a0, a1, a2, a3, bq.x, bq.y);
-              mma_f16(Dg[nt], a0, a1, a2, a3, bq.z, bq.w);
-            }
-          }
-          const float s0 = mk0[gq].x * code_unit, s1 = mk1[gq].x * code_unit;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float2 qs = *reinterpret_cast<const float2*>(&Qsum[gq * NQP + nt * 8 + 2 * c]);
-            Sref[nt][0] += s0 * Dg[nt][0] + mk0[gq].y * qs.x;
-            Sref[nt][1] += s0 * Dg[nt][1] + mk0[gq].y * qs.y;
-            Sref[nt][2] += s1 * Dg[nt][2] + mk1[gq].y * qs.x;
-            Sref[nt][3] += s1 * Dg[nt][3] + mk1[gq].y * qs.y;
-          }
-        }
-        // residuals of every loop of the block, one fragment
-        if (nr > 0) {
-          float Dr[NT][4];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) Dr[nt][k] = 0.f;
-#pragma unroll
-          for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
-            if (ri >= nr) break;
-            const int nt_ri = ((blk.r0 + ri - blk.lb) * blk.gw) >> 3;
-            const bool two = a.rbits[ri] == 2;
-            uint32_t wl, wh;
-            if (two) {
-              const int off = a.off_krc[ri] + ((c >> 1) * NG + gq) * 4;
-              wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
-              wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
-            } else {
-              const int off = a.off_krc[ri] + (c * NG + gq) * 4;
-              wl = lds32(sb + off + tr0 * RB4);
-              wh = lds32(sb + off + tr1 * RB4);
-            }
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              uint32_t a0, a1, a2, a3;
-              if (two) {
-                a_pairs_2bit(wl, s, a0, a2);
-                a_pairs_2bit(wh, s, a1, a3);
-              } else {
-                a_pairs_4bit(wl, s, a0, a2);
-                a_pairs_4bit(wh, s, a1, a3);
-              }
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (nt != nt_ri) continue;
-                const int fi = ((gq * 2 + s) * NT + nt) * 32 + lane;
-                const uint4 bq = sel4(riB[nt] == ri, (RES4 && !two) ? QR4[fi] : QR2[fi]);
-                mma_f16(Dr[nt], a0, a1, a2, a3, bq.x, bq.y);
-                mma_f16(Dr[nt], a0, a1, a2, a3, bq.z, bq.w);
-              }
-            }
-          }
-          // each column's own loop: its step and offset
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int ri = riD[nt][e];
-              const float2 m0 = ld_meta(sb + krmD[nt][e] + (tr0 * NG + gq) * 4);
-              const float2 m1 = ld_meta(sb + krmD[nt][e] + (tr1 * NG + gq) * 4);
-              const float qrs = QRsum[gq * NQP + nt * 8 + 2 * c + e];
-              const float d0 = (m0.x * code_unit) * Dr[nt][e] + m0.y * qrs;
-              const float d1 = (m1.x * code_unit) * Dr[nt][2 + e] + m1.y * qrs;
-              Sres[nt][e] += ri >= 0 ? d0 : 0.f;
-              Sres[nt][2 + e] += ri >= 0 ? d1 : 0.f;
-            }
-          }
-        }
-      }
-      // score = a_t * reference part + residual part (final loop: the reference alone)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ri = riD[nt][e];
-          float s_0 = Sref[nt][e], s_1 = Sref[nt][2 + e];
-          if (nr > 0) {
-            const float al0 = ld_half(sb + kaD[nt][e] + tr0 * 2);
-            const float al1 = ld_half(sb + kaD[nt][e] + tr1 * 2);
-            s_0 = ri >= 0 ? al0 * s_0 + Sres[nt][e] : s_0;
-            s_1 = ri >= 0 ? al1 * s_1 + Sres[nt][2 + e] : s_1;
-          }
-          sc[nt][e] = v0 ? s_0 : -INFINITY;
-          sc[nt][2 + e] = v1 ? s_1 : -INFINITY;
-        }
-      }
-    }
-    // per-warp column maxima over its 16 tokens
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float m0 = fmaxf(sc[nt][0], sc[nt][2]), m1 = fmaxf(sc[nt][1], sc[nt][3]);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        m0 = fmaxf(m0, __shfl_xor_sync(RQ_FULL_MASK, m0, o));
-        m1 = fmaxf(m1, __shfl_xor_sync(RQ_FULL_MASK, m1, o));
-      }
-      if (r == 0) {
-        red[warp * NQP + nt * 8 + 2 * c] = m0;
-        red[warp * NQP + nt * 8 + 2 * c + 1] = m1;
-      }
-    }
-    if (__syncthreads_or(!ok)) {  // (A)
+    if (!__all_sync(RQ_FULL_MASK,
+                    mbar_wait_bounded(smem_u32(&bars[st]), uint32_t((i / S) & 1), kWaitLimitNs))) {
       failed = true;
-      fail_tile = i;
       break;
     }
-    // ---------------------------------------------------------------- online softmax
-    float corr[NT][2];
-    float mnew_mine = 0.f;
-    if (threadIdx.x < NQP) {
-      float mt = red[threadIdx.x];
-#pragma unroll
-      for (int w = 1; w < kW; ++w) mt = fmaxf(mt, red[w * NQP + threadIdx.x]);
-      mnew_mine = fmaxf(mrun[threadIdx.x], mt);
-    }
-    // value-offset sums are kept per B-fragment column nt*8 + r
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int col = nt * 8 + r;
-      float mt = red[col];
-#pragma unroll
-      for (int w = 1; w < kW; ++w) mt = fmaxf(mt, red[w * NQP + col]);
-      const float mo = mrun[col];
-      const float cb = (mo == -INFINITY) ? 0.f : exp2f(mo - fmaxf(mo, mt));
-      offR[nt] *= cb;
-      offE[nt] *= cb;
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = nt * 8 + 2 * c + e;
-        float mt = red[col];
-#pragma unroll
-        for (int w = 1; w < kW; ++w) mt = fmaxf(mt, red[w * NQP + col]);
-        const float mo = mrun[col];
-        const float mn = fmaxf(mo, mt);
-        corr[nt][e] = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
-        const float p0 = exp2f(sc[nt][e] - mn), p1 = exp2f(sc[nt][2 + e] - mn);
-        lpart[nt][e] = lpart[nt][e] * corr[nt][e] + p0 + p1;
-        const int ri = riD[nt][e];
-        float a0v = 1.f, a1v = 1.f;
-        if (nr > 0) {
-          const float x0 = ld_half(sb + vaD[nt][e] + tr0 * 2);
-          const float x1 = ld_half(sb + vaD[nt][e] + tr1 * 2);
-          a0v = ri >= 0 ? x0 : 1.f;
-          a1v = ri >= 0 ? x1 : 1.f;
-        }
-        Ps[tr0 * PR + col] = v0 ? p0 : 0.f;
-        Ps[tr1 * PR + col] = v1 ? p1 : 0.f;
-        Pa[tr0 * PR + col] = v0 ? p0 * a0v : 0.f;
-        Pa[tr1 * PR + col] = v1 ? p1 * a1v : 0.f;
-      }
-    }
-    // the stage read by tile i-1 is free (every warp is past barrier A): refill it
-    if (threadIdx.x == 0 && i >= 1 && i + S - 1 < ntiles) {
-      issue(i + S - 1);
-      next_issue = i + S;
-    }
-    __syncthreads();  // (B)
-    if (threadIdx.x < NQP) mrun[threadIdx.x] = mnew_mine;
+    const uint8_t* sb = smem + st * a.stage_bytes;
+    const int t0 = t_begin + i * kT;
+    if (t0 + 16 * warp < t_end) {   // the warp has tokens in this tile
+      const bool v0 = t0 + tr0 < t_end, v1 = t0 + tr1 < t_end;
 
-    // ------------------------------------------------------------ values (one group/warp)
-#pragma unroll
-    for (int m = 0; m < MTW; ++m)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          accR[m][nt][k] *= corr[nt][k & 1];
-          accE2[m][nt][k] *= corr[nt][k & 1];
-          if (RES4) accE4[m][nt][k] *= corr[nt][k & 1];
-        }
-#pragma unroll
-    for (int ks = 0; ks < kT / 16; ++ks) {
-      int tt[4];
-      tt[0] = 16 * ks + 2 * c;
-      tt[1] = tt[0] + 1;
-      tt[2] = tt[0] + 8;
-      tt[3] = tt[0] + 9;
-      const int p0 = 8 * ks + c, p1 = p0 + 4;            // token pairs of this k-step
-      // reference values
+      // ---------------------------------------------------------------- scores
+      float sc[4];
       {
-        float2 vm[4];
+        float R[4], E[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) vm[k] = ld_meta(sb + a.off_vm + (tt[k] * NG + gv) * 4);
-        uint32_t bR[NT][4];
+        for (int k = 0; k < 4; ++k) R[k] = E[k] = 0.f;
+        uint32_t km0[NG], km1[NG], kw0[NG], kw1[NG];
+        load_words<NG>(sb + a.off_km + tr0 * NG * 4, km0);
+        load_words<NG>(sb + a.off_km + tr1 * NG * 4, km1);
+        // this lane's word of every group (K rows are group-interleaved: one load)
+        load_words<NG>(sb + a.off_kc + tr0 * RB4 + c * NG * 4, kw0);
+        load_words<NG>(sb + a.off_kc + tr1 * RB4 + c * NG * 4, kw1);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int n = nt * 8 + r;
-          float w[4];
+        for (int gq = 0; gq < NG; ++gq) {
+          {  // reference
+            float Dg[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float pa = Pa[tt[k] * PR + n];     // 0 for tokens past the context
-            w[k] = pa * vm[k].x;
-            offR[nt] += pa * vm[k].y;
+            for (int s = 0; s < 2; ++s) {
+              uint32_t a0, a2, a1, a3;
+              a_pairs_4bit(kw0[gq], s, a0, a2);
+              a_pairs_4bit(kw1[gq], s, a1, a3);
+              const uint4 bq = QF[(gq * 2 + s) * 32 + lane];
+              mma_f16(Dg, a0, a1, a2, a3, bq.x, bq.y);
+              mma_f16(Dg, a0, a1, a2, a3, bq.z, bq.w);
+            }
+            const float2 m0 = meta_f2(km0[gq]), m1 = meta_f2(km1[gq]);
+            const float2 qs = *reinterpret_cast<const float2*>(&Qsum[gq * NQ + 2 * c]);
+            R[0] = fmaf(m0.x, Dg[0], fmaf(m0.y, qs.x, R[0]));
+            R[1] = fmaf(m0.x, Dg[1], fmaf(m0.y, qs.y, R[1]));
+            R[2] = fmaf(m1.x, Dg[2], fmaf(m1.y, qs.x, R[2]));
+            R[3] = fmaf(m1.x, Dg[3], fmaf(m1.y, qs.y, R[3]));
           }
-          split_half2(w[0], w[1], bR[nt][0], bR[nt][2]);
-          split_half2(w[2], w[3], bR[nt][1], bR[nt][3]);
+          if (nr > 0) {  // residuals of every loop of the block
+            float dsel[4];
+            if constexpr (PER_LOOP) {
+              const uint4 q2s0 = QR2[(gq * 2 + 0) * 32 + lane];
+              const uint4 q2s1 = QR2[(gq * 2 + 1) * 32 + lane];
+              uint4 q4s0 = make_uint4(0u, 0u, 0u, 0u), q4s1 = q4s0;
+              if (RES4) {
+                q4s0 = QR4[(gq * 2 + 0) * 32 + lane];
+                q4s1 = QR4[(gq * 2 + 1) * 32 + lane];
+              }
+              float Dr[PER_LOOP ? NRT : 1][4];
+#pragma unroll
+              for (int ri = 0; ri < NRT; ++ri) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) Dr[ri][k] = 0.f;
+                const bool two = !RES4 || a.rbits[ri] == 2;   // without 4-bit loops: all 2-bit
+                uint32_t wl, wh;
+                if (two) {
+                  const int off = a.off_krc[ri] + ((c >> 1) * NG + gq) * 4;
+                  wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
+                  wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
+                } else {
+                  const int off = a.off_krc[ri] + (c * NG + gq) * 4;
+                  wl = lds32(sb + off + tr0 * RB4);
+                  wh = lds32(sb + off + tr1 * RB4);
+                }
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                  uint32_t a0, a1, a2, a3;
+                  if (two) {
+                    a_pairs_2bit(wl, s, a0, a2);
+                    a_pairs_2bit(wh, s, a1, a3);
+                  } else {
+                    a_pairs_4bit(wl, s, a0, a2);
+                    a_pairs_4bit(wh, s, a1, a3);
+                  }
+                  const uint4 bq = (RES4 && !two) ? (s ? q4s1 : q4s0) : (s ? q2s1 : q2s0);
+                  mma_f16(Dr[ri], a0, a1, a2, a3, bq.x, bq.y);
+                  mma_f16(Dr[ri], a0, a1, a2, a3, bq.z, bq.w);
+                }
+              }
+              // each column keeps its own loop's product
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                float d = Dr[0][k];
+#pragma unroll
+                for (int ri = 1; ri < NRT; ++ri) d = blend(loop_mask[k & 1][ri], Dr[ri][k], d);
+                dsel[k] = d;
+              }
+            } else {
+              // run-time loop count: one accumulator, query fragments masked to each loop's
+              // columns
+              float Dr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
+                if (ri >= nr) break;
+                const bool two = !RES4 || a.rbits[ri] == 2;
+                uint32_t wl, wh;
+                if (two) {
+                  const int off = a.off_krc[ri] + ((c >> 1) * NG + gq) * 4;
+                  wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
+                  wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
+                } else {
+                  const int off = a.off_krc[ri] + (c * NG + gq) * 4;
+                  wl = lds32(sb + off + tr0 * RB4);
+                  wh = lds32(sb + off + tr1 * RB4);
+                }
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                  uint32_t a0, a1, a2, a3;
+                  if (two) {
+                    a_pairs_2bit(wl, s, a0, a2);
+                    a_pairs_2bit(wh, s, a1, a3);
+                  } else {
+                    a_pairs_4bit(wl, s, a0, a2);
+                    a_pairs_4bit(wh, s, a1, a3);
+                  }
+                  const int fi = (gq * 2 + s) * 32 + lane;
+                  const uint4 bq = sel4(riB == ri, (RES4 && !two) ? QR4[fi] : QR2[fi]);
+                  mma_f16(Dr, a0, a1, a2, a3, bq.x, bq.y);
+                  mma_f16(Dr, a0, a1, a2, a3, bq.z, bq.w);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dsel[k] = Dr[k];
+            }
+            // each column's own loop: its step and offset
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float2 m0 = ld_meta(sb + krmD[e] + (tr0 * NG + gq) * 4);
+              const float2 m1 = ld_meta(sb + krmD[e] + (tr1 * NG + gq) * 4);
+              const float qrs = QRsum[gq * NQ + 2 * c + e];
+              E[e] = fmaf(m0.x, dsel[e], fmaf(m0.y, qrs, E[e]));
+              E[2 + e] = fmaf(m1.x, dsel[2 + e], fmaf(m1.y, qrs, E[2 + e]));
+            }
+          }
         }
-        const uint32_t W0 = lds32(sb + a.off_vc + p0 * D + ((8 * gv + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
-        const uint32_t W1 = lds32(sb + a.off_vc + p1 * D + ((8 * gv + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
+        // score = a_t * reference part + residual part (final loop: the reference alone)
 #pragma unroll
-        for (int m = 0; m < MTW; ++m) {
-          const int mtg = (D == 128) ? m : (warp & 1);
-          uint32_t a0, a1, a2, a3;
-          a_pairs_4bit<true>(W0, mtg, a0, a1);
-          a_pairs_4bit<true>(W1, mtg, a2, a3);
+        for (int e = 0; e < 2; ++e) {
+          float s_0 = R[e], s_1 = R[2 + e];
+          if (nr > 0) {
+            const float al0 = ld_half(sb + kaD[e] + tr0 * 2);
+            const float al1 = ld_half(sb + kaD[e] + tr1 * 2);
+            s_0 = riD[e] >= 0 ? fmaf(al0, s_0, E[e]) : s_0;
+            s_1 = riD[e] >= 0 ? fmaf(al1, s_1, E[2 + e]) : s_1;
+          }
+          sc[e] = v0 ? s_0 * code_unit : -INFINITY;
+          sc[2 + e] = v1 ? s_1 * code_unit : -INFINITY;
+        }
+      }
+
+      // ---------------------------------------------------------------- online softmax
+      float p[4];
+      {
+        float tm[2];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_f16(accR[m][nt], a0, a1, a2, a3, bR[nt][0], bR[nt][1]);
-            mma_f16(accR[m][nt], a0, a1, a2, a3, bR[nt][2], bR[nt][3]);
+        for (int e = 0; e < 2; ++e) {
+          float m = fmaxf(sc[e], sc[2 + e]);
+          m = fmaxf(m, __shfl_xor_sync(RQ_FULL_MASK, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(RQ_FULL_MASK, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(RQ_FULL_MASK, m, 16));
+          tm[e] = m;
+        }
+        const bool n0 = tm[0] > mw[0] + kRescaleSlack, n1 = tm[1] > mw[1] + kRescaleSlack;
+        if (__any_sync(RQ_FULL_MASK, n0 || n1)) {
+          float corr[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float mn = (e ? n1 : n0) ? tm[e] : mw[e];
+            corr[e] = (mw[e] == -INFINITY) ? 0.f : exp2f(mw[e] - mn);
+            mw[e] = mn;
+            lsum[e] *= corr[e];
+          }
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              accR[m][k] *= corr[k & 1];
+              accE2[m][k] *= corr[k & 1];
+              if (RES4) accE4[m][k] *= corr[k & 1];
+            }
+#pragma unroll
+          for (int g = 0; g < NG; ++g)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              offR[g][e] *= corr[e];
+              offE[g][e] *= corr[e];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) p[k] = (sc[k] == -INFINITY) ? 0.f : exp2f(sc[k] - mw[k & 1]);
+        lsum[0] += p[0] + p[2];
+        lsum[1] += p[1] + p[3];
+      }
+
+      // ---------------------------------------------------------------- values
+      {
+        // p * a (reference weights before the step) and p (residual weights before the step)
+        // of this lane's score elements; slots past the context may hold any bits
+        float pa[4], pe[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float x0 = 1.f, x1 = 1.f;
+          if (nr > 0) {
+            const float y0 = ld_half(sb + vaD[e] + tr0 * 2);
+            const float y1 = ld_half(sb + vaD[e] + tr1 * 2);
+            x0 = riD[e] >= 0 ? y0 : 1.f;
+            x1 = riD[e] >= 0 ? y1 : 1.f;
+          }
+          pa[e] = v0 ? p[e] * x0 : 0.f;
+          pa[2 + e] = v1 ? p[2 + e] * x1 : 0.f;
+          pe[e] = (v0 && riD[e] >= 0) ? p[e] : 0.f;
+          pe[2 + e] = (v1 && riD[e] >= 0) ? p[2 + e] : 0.f;
+        }
+        uint32_t vm0[NG], vm1[NG];
+        load_words<NG>(sb + a.off_vm + tr0 * NG * 4, vm0);
+        load_words<NG>(sb + a.off_vm + tr1 * NG * 4, vm1);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          vm0[g] = v0 ? vm0[g] : 0u;
+          vm1[g] = v1 ? vm1[g] : 0u;
+        }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const float2 m0 = meta_f2(vm0[g]), m1 = meta_f2(vm1[g]);
+          offR[g][0] = fmaf(pa[0], m0.y, fmaf(pa[2], m1.y, offR[g][0]));
+          offR[g][1] = fmaf(pa[1], m0.y, fmaf(pa[3], m1.y, offR[g][1]));
+          uint32_t bh0, bh1, bl0, bl1;
+          weights_to_b(pa[0] * m0.x, pa[1] * m0.x, pa[2] * m1.x, pa[3] * m1.x, bh0, bh1, bl0, bl1);
+          const uint32_t W0 = lds32(sb + a.off_vc + p0 * D + ((8 * g + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
+          const uint32_t W1 = lds32(sb + a.off_vc + p1 * D + ((8 * g + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
+#pragma unroll
+          for (int mtg = 0; mtg < 2; ++mtg) {
+            uint32_t x0, x1, x2, x3;
+            a_pairs_4bit<true>(W0, mtg, x0, x1);
+            a_pairs_4bit<true>(W1, mtg, x2, x3);
+            mma_f16(accR[2 * g + mtg], x0, x1, x2, x3, bh0, bh1);
+            mma_f16(accR[2 * g + mtg], x0, x1, x2, x3, bl0, bl1);
+          }
+        }
+        if (nr > 0) {
+          // each D column's own loop: its value step and offset, tokens tr0 and tr1
+          uint32_t rm0[2][NG], rm1[2][NG];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            load_words<NG>(sb + vrmD[e] + tr0 * NG * 4, rm0[e]);
+            load_words<NG>(sb + vrmD[e] + tr1 * NG * 4, rm1[e]);
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+              rm0[e][g] = v0 ? rm0[e][g] : 0u;
+              rm1[e][g] = v1 ? rm1[e][g] : 0u;
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            float w[4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float2 m0 = meta_f2(rm0[e][g]), m1 = meta_f2(rm1[e][g]);
+              w[e] = pe[e] * m0.x;
+              w[2 + e] = pe[2 + e] * m1.x;
+              offE[g][e] = fmaf(pe[e], m0.y, fmaf(pe[2 + e], m1.y, offE[g][e]));
+            }
+            uint32_t bh0, bh1, bl0, bl1;
+            weights_to_b(w[0], w[1], w[2], w[3], bh0, bh1, bl0, bl1);
+#pragma unroll
+            for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
+              if (ri >= nr) break;
+              // weights of the other loops' columns are masked (one loop: nothing to mask)
+              const bool keep = (NRT == 1) || (riB == ri);
+              const uint32_t eh0 = keep ? bh0 : 0u, eh1 = keep ? bh1 : 0u;
+              const uint32_t el0 = keep ? bl0 : 0u, el1 = keep ? bl1 : 0u;
+              if (!RES4 || a.rbits[ri] == 2) {
+                const int sh = 8 * (r & 1);
+                const int u = 4 * g + (r >> 1);
+                const uint32_t W0 =
+                    lds32(sb + a.off_vrc[ri] + p0 * (2 * RB2) + (u ^ v_unit_swizzle(p0, D / 8)) * 4) >> sh;
+                const uint32_t W1 =
+                    lds32(sb + a.off_vrc[ri] + p1 * (2 * RB2) + (u ^ v_unit_swizzle(p1, D / 8)) * 4) >> sh;
+#pragma unroll
+                for (int mtg = 0; mtg < 2; ++mtg) {
+                  uint32_t x0, x1, x2, x3;
+                  a_pairs_2bit<true>(W0, mtg, x0, x1);
+                  a_pairs_2bit<true>(W1, mtg, x2, x3);
+                  mma_f16(accE2[2 * g + mtg], x0, x1, x2, x3, eh0, eh1);
+                  mma_f16(accE2[2 * g + mtg], x0, x1, x2, x3, el0, el1);
+                }
+              } else if (RES4) {
+                const uint32_t W0 =
+                    lds32(sb + a.off_vrc[ri] + p0 * D + ((8 * g + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
+                const uint32_t W1 =
+                    lds32(sb + a.off_vrc[ri] + p1 * D + ((8 * g + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
+#pragma unroll
+                for (int mtg = 0; mtg < 2; ++mtg) {
+                  uint32_t x0, x1, x2, x3;
+                  a_pairs_4bit<true>(W0, mtg, x0, x1);
+                  a_pairs_4bit<true>(W1, mtg, x2, x3);
+                  mma_f16(accE4[RES4 ? 2 * g + mtg : 0], x0, x1, x2, x3, eh0, eh1);
+                  mma_f16(accE4[RES4 ? 2 * g + mtg : 0], x0, x1, x2, x3, el0, el1);
+                }
+              }
+            }
           }
         }
       }
-      // residual values: one set of weights per column (its own loop's step)
-      if (nr > 0) {
-        uint4 bE[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int n = nt * 8 + r;
-          const int ri = riB[nt];
-          float w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 mm = ld_meta(sb + vrmB[nt] + (tt[k] * NG + gv) * 4);
-            const float ps = ri >= 0 ? Ps[tt[k] * PR + n] : 0.f;
-            w[k] = ps * mm.x;
-            offE[nt] += ps * mm.y;
-          }
-          split_half2(w[0], w[1], bE[nt].x, bE[nt].z);
-          split_half2(w[2], w[3], bE[nt].y, bE[nt].w);
-        }
-#pragma unroll
-        for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
-          if (ri >= nr) break;
-          const int nt_ri = ((blk.r0 + ri - blk.lb) * blk.gw) >> 3;
-          if (a.rbits[ri] == 2) {
-            const int sh = 8 * (r & 1);
-            const int u = 4 * gv + (r >> 1);
-            const uint32_t W0 =
-                lds32(sb + a.off_vrc[ri] + p0 * (2 * RB2) + (u ^ v_unit_swizzle(p0, D / 8)) * 4) >> sh;
-            const uint32_t W1 =
-                lds32(sb + a.off_vrc[ri] + p1 * (2 * RB2) + (u ^ v_unit_swizzle(p1, D / 8)) * 4) >> sh;
-#pragma unroll
-            for (int m = 0; m < MTW; ++m) {
-              const int mtg = (D == 128) ? m : (warp & 1);
-              uint32_t a0, a1, a2, a3;
-              a_pairs_2bit<true>(W0, mtg, a0, a1);
-              a_pairs_2bit<true>(W1, mtg, a2, a3);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (nt != nt_ri) continue;
-                const uint4 bb = sel4(riB[nt] == ri, bE[nt]);
-                mma_f16(accE2[m][nt], a0, a1, a2, a3, bb.x, bb.y);
-                mma_f16(accE2[m][nt], a0, a1, a2, a3, bb.z, bb.w);
-              }
-            }
-          } else if (RES4) {
-            const uint32_t W0 =
-                lds32(sb + a.off_vrc[ri] + p0 * D + ((8 * gv + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
-            const uint32_t W1 =
-                lds32(sb + a.off_vrc[ri] + p1 * D + ((8 * gv + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
-#pragma unroll
-            for (int m = 0; m < MTW; ++m) {
-              const int mtg = (D == 128) ? m : (warp & 1);
-              uint32_t a0, a1, a2, a3;
-              a_pairs_4bit<true>(W0, mtg, a0, a1);
-              a_pairs_4bit<true>(W1, mtg, a2, a3);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (nt != nt_ri) continue;
-                const uint4 bb = sel4(riB[nt] == ri, bE[nt]);
-                mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, bb.x, bb.y);
-                mma_f16(accE4[RES4 ? m : 0][nt], a0, a1, a2, a3, bb.z, bb.w);
-              }
-            }
-          }
+    }
+    // this warp is done with the stage; the last of the four refills it
+    __syncwarp();
+    if (lane == 0) {
+      if (atom_add_acq_rel(&cnt[st], 1u) == unsigned(kW - 1)) {
+        cnt[st] = 0u;
+        if (i + S < ntiles) {
+          fence_proxy_async_smem();
+          issue(i + S);
+          cnt[kIssuedSlot] = unsigned(i + S + 1);
         }
       }
     }
@@ -677,33 +729,78 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
     // a copy never completed: flag it, wait (bounded) for the copies still in flight, leave
     if (threadIdx.x == 0) {
       atomicOr(a.err, 1u);
-      for (int t = fail_tile; t < next_issue; ++t)
+      const int issued = int(cnt[kIssuedSlot]);
+      for (int t = issued - S < 0 ? 0 : issued - S; t < issued; ++t)
         mbar_wait_bounded(smem_u32(&bars[t % S]), uint32_t((t / S) & 1), kWaitLimitNs);
     }
     __syncthreads();
     return;
   }
 
-  // ------------------------------------------------------------------ split partials
-  // softmax sums: over the 8 row lanes, then over the warps
+  // ------------------------------------------------------------------ merge the four warps
+  // every issued copy has landed and been consumed: the stage memory is free
+  // softmax sums and value offsets: over the 8 row lanes (tokens)
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int e = 0; e < 2; ++e) {
+    float v = lsum[e];
+    v += __shfl_xor_sync(RQ_FULL_MASK, v, 4);
+    v += __shfl_xor_sync(RQ_FULL_MASK, v, 8);
+    v += __shfl_xor_sync(RQ_FULL_MASK, v, 16);
+    lsum[e] = v;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float v = lpart[nt][e];
-      v += __shfl_xor_sync(RQ_FULL_MASK, v, 4);
-      v += __shfl_xor_sync(RQ_FULL_MASK, v, 8);
-      v += __shfl_xor_sync(RQ_FULL_MASK, v, 16);
-      if (r == 0) red[warp * NQP + nt * 8 + 2 * c + e] = v;
+    for (int g = 0; g < NG; ++g) {
+      float x = offR[g][e], y = offE[g][e];
+      x += __shfl_xor_sync(RQ_FULL_MASK, x, 4);
+      y += __shfl_xor_sync(RQ_FULL_MASK, y, 4);
+      x += __shfl_xor_sync(RQ_FULL_MASK, x, 8);
+      y += __shfl_xor_sync(RQ_FULL_MASK, y, 8);
+      x += __shfl_xor_sync(RQ_FULL_MASK, x, 16);
+      y += __shfl_xor_sync(RQ_FULL_MASK, y, 16);
+      offR[g][e] = x;
+      offE[g][e] = y;
     }
-  // value offsets: over the 4 token lanes of each column
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    offR[nt] += __shfl_xor_sync(RQ_FULL_MASK, offR[nt], 1);
-    offR[nt] += __shfl_xor_sync(RQ_FULL_MASK, offR[nt], 2);
-    offE[nt] += __shfl_xor_sync(RQ_FULL_MASK, offE[nt], 1);
-    offE[nt] += __shfl_xor_sync(RQ_FULL_MASK, offE[nt], 2);
   }
+  if (r == 0) {
+    red[warp * NQ + 2 * c] = mw[0];
+    red[warp * NQ + 2 * c + 1] = mw[1];
+  }
+  __syncthreads();
+  float f[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float M = red[2 * c + e];
+#pragma unroll
+    for (int w = 1; w < kW; ++w) M = fmaxf(M, red[w * NQ + 2 * c + e]);
+    f[e] = (mw[e] == -INFINITY) ? 0.f : exp2f(mw[e] - M);
+  }
+  if (r == 0) {
+    red[kW * NQ + warp * NQ + 2 * c] = lsum[0] * f[0];
+    red[kW * NQ + warp * NQ + 2 * c + 1] = lsum[1] * f[1];
+  }
+  // this warp's rescaled partial accumulators: buf[warp][column][acc_ref D | acc_res D]
+  float* buf = reinterpret_cast<float*>(smem);
+  // channels of this thread: 32 g + 4 r + 2 mtg + hh; columns 2c + e
+#pragma unroll
+  for (int g = 0; g < NG; ++g)
+#pragma unroll
+    for (int mtg = 0; mtg < 2; ++mtg)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {          // hh: row r (j even) or row r+8 (j odd)
+        const int j = 2 * mtg + hh;
+        const int ch = 32 * g + 4 * r + j;
+        const float sc4 = hh ? 0.0625f : 1.f;     // value codes are normal fp16
+        const float sc2 = 1.f / float(1 << (2 * j));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 2 * hh + e;
+          const float vr = fmaf(accR[2 * g + mtg][k], sc4, offR[g][e]);
+          float ve = fmaf(accE2[2 * g + mtg][k], sc2, offE[g][e]);
+          if (RES4) ve = fmaf(accE4[RES4 ? 2 * g + mtg : 0][k], sc4, ve);
+          float* o = buf + (warp * NQ + 2 * c + e) * (2 * D);
+          o[ch] = vr * f[e];
+          o[D + ch] = ve * f[e];
+        }
+      }
   __syncthreads();
   const int rec = int(partial_floats_d(D));
   auto rec_ptr = [&](int col) -> float* {
@@ -713,43 +810,26 @@ __global__ void __launch_bounds__(kW * 32) rq_mma_kernel(const __grid_constant__
     const int64_t hq = int64_t(h) * a.g + gi;
     return a.part + (((int64_t(b) * a.Hq + hq) * a.loop_count + lc) * a.n_splits + split) * rec;
   };
-  if (threadIdx.x < NQP) {
+  if (threadIdx.x < NQ) {
     float* o = rec_ptr(threadIdx.x);
     if (o) {
-      float ls = 0.f;
+      float M = red[threadIdx.x], ls = 0.f;
 #pragma unroll
-      for (int w = 0; w < kW; ++w) ls += red[w * NQP + threadIdx.x];
-      o[0] = mrun[threadIdx.x];
+      for (int w = 1; w < kW; ++w) M = fmaxf(M, red[w * NQ + threadIdx.x]);
+#pragma unroll
+      for (int w = 0; w < kW; ++w) ls += red[kW * NQ + w * NQ + threadIdx.x];
+      o[0] = M;
       o[1] = ls;
     }
   }
-  // channels of this thread: 32 gv + 4 r + 2 mtg + {0, 1}; columns nt*8 + 2c + {0, 1}
+  for (int idx = threadIdx.x; idx < NQ * 2 * D; idx += kW * 32) {
+    const int col = idx / (2 * D), k = idx % (2 * D);
+    float* o = rec_ptr(col);
+    if (!o) continue;
+    float v = 0.f;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int col = nt * 8 + 2 * c + e;
-      const float oR = __shfl_sync(RQ_FULL_MASK, offR[nt], (2 * c + e) * 4);
-      const float oE = __shfl_sync(RQ_FULL_MASK, offE[nt], (2 * c + e) * 4);
-      float* o = rec_ptr(col);
-      if (!o) continue;
-#pragma unroll
-      for (int m = 0; m < MTW; ++m) {
-        const int mtg = (D == 128) ? m : (warp & 1);
-        const int ch = 32 * gv + 4 * r + 2 * mtg;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {      // hh: row r (j even) or row r+8 (j odd)
-          const int j = 2 * mtg + hh;
-          const float sc4 = (j & 1) ? 0.0625f : 1.f;      // value codes are normal fp16
-          const float sc2 = 1.f / float(1 << (2 * j));
-          const float vr = accR[m][nt][2 * hh + e] * sc4 + oR;
-          float ve = accE2[m][nt][2 * hh + e] * sc2 + oE;
-          if (RES4) ve += accE4[RES4 ? m : 0][nt][2 * hh + e] * sc4;
-          o[4 + ch + hh] = vr;
-          o[4 + D + ch + hh] = ve;
-        }
-      }
-    }
+    for (int w = 0; w < kW; ++w) v += buf[(w * NQ + col) * (2 * D) + k];
+    o[4 + k] = v;
   }
 }
 
@@ -757,29 +837,28 @@ using KernelFn = void (*)(MmaArgs);
 
 template <int D>
 KernelFn pick_generic(bool res4) {
-  return res4 ? rq_mma_kernel<D, 1, true, -1> : rq_mma_kernel<D, 1, false, -1>;
+  return res4 ? rq_mma_kernel<D, true, -1> : rq_mma_kernel<D, false, -1>;
 }
 
 // Variants with the residual-loop count fixed at compile time, for the common blocks: one
 // loop of a per-loop call (0 or 1 residual), two loops of a 4-query-head GQA block (2) and
 // all four loops of a 4-loop model (3).
-KernelFn pick(int D, int nt, bool res4, int nr) {
-  if (D == 128 && nt == 1 && !res4) {
-    if (nr == 0) return rq_mma_kernel<128, 1, false, 0>;
-    if (nr == 1) return rq_mma_kernel<128, 1, false, 1>;
-    if (nr == 2) return rq_mma_kernel<128, 1, false, 2>;
-    if (nr == 3) return rq_mma_kernel<128, 1, false, 3>;
+KernelFn pick(int D, bool res4, int nr) {
+  if (D == 128 && !res4) {
+    if (nr == 0) return rq_mma_kernel<128, false, 0>;
+    if (nr == 1) return rq_mma_kernel<128, false, 1>;
+    if (nr == 2) return rq_mma_kernel<128, false, 2>;
+    if (nr == 3) return rq_mma_kernel<128, false, 3>;
   }
-  if (D == 128 && nt == 1 && res4) {
-    if (nr == 1) return rq_mma_kernel<128, 1, true, 1>;
-    if (nr == 3) return rq_mma_kernel<128, 1, true, 3>;
+  if (D == 128 && res4) {
+    if (nr == 1) return rq_mma_kernel<128, true, 1>;
+    if (nr == 3) return rq_mma_kernel<128, true, 3>;
   }
-  if (D == 64 && nt == 1 && !res4) {
-    if (nr == 0) return rq_mma_kernel<64, 1, false, 0>;
-    if (nr == 1) return rq_mma_kernel<64, 1, false, 1>;
-    if (nr == 3) return rq_mma_kernel<64, 1, false, 3>;
+  if (D == 64 && !res4) {
+    if (nr == 0) return rq_mma_kernel<64, false, 0>;
+    if (nr == 1) return rq_mma_kernel<64, false, 1>;
+    if (nr == 3) return rq_mma_kernel<64, false, 3>;
   }
-  (void)nt;                                     // blocks hold one n-tile (8 columns)
   return D == 128 ? pick_generic<128>(res4) : pick_generic<64>(res4);
 }
 
@@ -792,23 +871,22 @@ cudaError_t prepare_kernels() {
   std::call_once(once[dev], [&] {
     err[dev] = cudaSuccess;
     for (int D : {64, 128})
-      for (int nt : {1})
-        for (bool r4 : {false, true})
-          for (int nr = -1; nr <= kMaxResPerBlock; ++nr) {
-            cudaError_t e = cudaFuncSetAttribute(pick(D, nt, r4, nr),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 200 * 1024);
-            if (e != cudaSuccess) err[dev] = e;
-          }
+      for (bool r4 : {false, true})
+        for (int nr = -1; nr <= kMaxResPerBlock; ++nr) {
+          cudaError_t e = cudaFuncSetAttribute(pick(D, r4, nr),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               200 * 1024);
+          if (e != cudaSuccess) err[dev] = e;
+        }
   });
   return err[dev];
 }
 
 // CTAs of a kernel variant resident per SM with `smem` bytes of dynamic shared memory.
-int resident_ctas(int D, int nt, bool res4, int nr, size_t smem) {
+int resident_ctas(int D, bool res4, int nr, size_t smem) {
   int n = 0;
   if (prepare_kernels() == cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, nt, res4, nr), kW * 32, smem) ==
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, res4, nr), kW * 32, smem) ==
           cudaSuccess &&
       n > 0)
     return n;
@@ -818,7 +896,6 @@ int resident_ctas(int D, int nt, bool res4, int nr, size_t smem) {
 
 struct BlockLaunch {
   MmaArgs a;
-  int nt;
   bool res4;
   size_t smem;
 };
@@ -858,15 +935,13 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
   }
   a.stage_bytes = off;
   a.blk = bq;
-  const int nq = bq.gw * bq.nl;
-  bl.nt = nq <= 8 ? 1 : (nq <= 16 ? 2 : 4);
   bl.res4 = res4;
   // most resident CTAs per SM first (latency hiding), then the deepest pipeline
   int best_ctas = 0;
   for (int stages = 3; stages >= 2; --stages) {
-    const size_t sm = smem_layout(D, bl.nt, res4, stages, a.stage_bytes).total;
+    const size_t sm = smem_layout(D, res4, stages, a.stage_bytes).total;
     if (sm > 200 * 1024) continue;
-    const int ctas = resident_ctas(D, bl.nt, res4, bq.nr, sm);
+    const int ctas = resident_ctas(D, res4, bq.nr, sm);
     if (ctas > best_ctas) {
       best_ctas = ctas;
       a.n_stages = stages;
@@ -876,13 +951,12 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
   return best_ctas > 0;
 }
 
-
 }  // namespace
 
 // Query columns per launch: one 8-column n-tile keeps registers and shared memory low enough
 // for three resident CTAs per SM; wider blocks (which read the reference tile once for more
 // loops) measured slower on GB300 because of the lower occupancy.
-constexpr int kMaxBlockColumns = 8;
+constexpr int kMaxBlockColumns = kNQ;
 
 int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* out, int max_out) {
   int gw = 1;
@@ -925,7 +999,7 @@ SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int 
   for (int i = 0; i < nb; ++i) {
     BlockLaunch bl;
     if (!build_block(s, dummy, blocks[i], bl)) continue;
-    const int n = resident_ctas(s.head_dim, bl.nt, bl.res4, blocks[i].nr, bl.smem);
+    const int n = resident_ctas(s.head_dim, bl.res4, blocks[i].nr, bl.smem);
     if (ctas == 0 || n < ctas) ctas = n;
   }
   return plan_splits_for(s, max_ctx, ctas > 0 ? ctas : 1, kT);
@@ -963,7 +1037,7 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.tokens_per_split = tokens_per_split;
     a.scale_log2 = scale * kLog2e;
     dim3 grid(n_splits, s.n_kv_heads, s.batch);
-    pick(s.head_dim, bl.nt, bl.res4, blocks[bi].nr)<<<grid, kW * 32, bl.smem, stream>>>(a);
+    pick(s.head_dim, bl.res4, blocks[bi].nr)<<<grid, kW * 32, bl.smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

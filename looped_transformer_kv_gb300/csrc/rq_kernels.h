@@ -17,30 +17,27 @@ struct QueryBlock {
   int gi0, gw, lb, nl, r0, nr;
 };
 
-// Shared-memory layout of the tensor-core decode kernel (byte offsets).  Rows of the
-// softmax-weight tables are padded by 4 floats so the value-phase fragment loads of the 4
-// token lanes of a column fall in distinct banks.
+// Shared-memory layout of the tensor-core decode kernel (byte offsets).  The stage region
+// also holds the four warps' partial accumulators when the tiles are done.
 struct SmemLayout {
-  int qf, qr2, qr4, qsum, qrsum, ps, pa, red, mrun, bars, total, prow;
+  int qf, qr2, qr4, qsum, qrsum, red, cnt, bars, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int D, int NT, bool res4, int stages,
-                                                  int stage_bytes) {
-  const int NG = D / 32, NQP = NT * 8;
+__host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, int stage_bytes) {
+  const int NG = D / 32, NQ = 8, W = 4;
   SmemLayout s;
-  s.prow = NQP + 4;
   int o = stages * stage_bytes;
+  const int merge = W * NQ * 2 * D * 4;
+  if (o < merge) o = merge;
   o = (o + 15) & ~15;
-  const int frag = NG * 2 * NT * 32 * 16;   // hi and lo f16x2 pairs per lane
+  const int frag = NG * 2 * 32 * 16;   // hi and lo f16x2 pairs per lane
   s.qf = o;    o += frag;
   s.qr2 = o;   o += frag;
   s.qr4 = o;   o += res4 ? frag : 0;
-  s.qsum = o;  o += NG * NQP * 4;
-  s.qrsum = o; o += NG * NQP * 4;
-  s.ps = o;    o += 64 * s.prow * 4;
-  s.pa = o;    o += 64 * s.prow * 4;
-  s.red = o;   o += 4 * NQP * 4;
-  s.mrun = o;  o += NQP * 4;
+  s.qsum = o;  o += NG * NQ * 4;
+  s.qrsum = o; o += NG * NQ * 4;
+  s.red = o;   o += 2 * W * NQ * 4;
+  s.cnt = o;   o += 16 * 4;           // stage release counters, tiles issued
   o = (o + 7) & ~7;
   s.bars = o;  o += stages * 8;
   s.total = o;
