@@ -197,7 +197,28 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
   const QueryBlock blk = a.blk;
   const int nr = NRT >= 0 ? NRT : blk.nr;
 
-  const SmemLayout lay = smem_layout(D, RES4, a.n_stages, a.stage_bytes);
+  // Stage layout (byte offsets within a stage): K codes, K steps, V codes, V steps, then per
+  // residual loop K codes, K steps, K a, V codes, V steps, V a.  Fixed at compile time when
+  // the residual-loop count is and every residual loop is 2-bit (for up to two residual
+  // loops: with three, the constant addresses cost more registers than they save).
+  constexpr bool FIXED = !RES4 && NRT >= 0 && NRT <= 2;
+  constexpr int F_KM = kT * RB4, F_VC = F_KM + kT * NG * 4, F_VM = F_VC + kT * RB4;
+  constexpr int F_RES = F_VM + kT * NG * 4;
+  constexpr int F_KRM = kT * RB2, F_KA = F_KRM + kT * NG * 4, F_VRC = F_KA + kT * 2;
+  constexpr int F_VRM = F_VRC + kT * RB2, F_VA = F_VRM + kT * NG * 4, F_RS = F_VA + kT * 2;
+  const int o_kc = FIXED ? 0 : a.off_kc;
+  const int o_km = FIXED ? F_KM : a.off_km;
+  const int o_vc = FIXED ? F_VC : a.off_vc;
+  const int o_vm = FIXED ? F_VM : a.off_vm;
+  const int SB = FIXED ? F_RES + (NRT >= 0 ? NRT : 0) * F_RS : a.stage_bytes;
+  auto o_krc = [&](int ri) { return FIXED ? F_RES + ri * F_RS : a.off_krc[ri]; };
+  auto o_vrc = [&](int ri) { return FIXED ? F_RES + ri * F_RS + F_VRC : a.off_vrc[ri]; };
+
+  if (FIXED && SB != a.stage_bytes) {   // host and kernel disagree on the layout: refuse
+    if (threadIdx.x == 0) atomicOr(a.err, 1u);
+    return;
+  }
+  const SmemLayout lay = smem_layout(D, RES4, a.n_stages, SB);
   uint4* QF = reinterpret_cast<uint4*>(smem + lay.qf);
   uint4* QR2 = reinterpret_cast<uint4*>(smem + lay.qr2);
   uint4* QR4 = reinterpret_cast<uint4*>(smem + lay.qr4);
@@ -260,14 +281,8 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
   }
 
   // ------------------------------------------------------------------ query preparation
-  {
-    uint32_t* z32 = reinterpret_cast<uint32_t*>(smem + lay.qf);
-    const int nz = (lay.cnt - lay.qf) / 4;
-    for (int i = threadIdx.x; i < nz; i += blockDim.x) z32[i] = 0u;
-  }
-  __syncthreads();
-  // query columns of this block: scaled q, rotated q' = R q, per-group sums
-  auto prep_column = [&](int n, float (&v)[P], float (&rr)[P]) -> bool {
+  // query columns of this block, two per warp: scaled q, rotated q' = R q, per-group sums
+  auto prep_column = [&](int n, float (&v)[P], float (&rr)[P]) {
     const int li = n / blk.gw;
     const int gi = blk.gi0 + n % blk.gw;
     const bool real = li < blk.nl && gi < a.g;
@@ -289,19 +304,26 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
     const float inv_sqrt_d = (D == 128) ? 0.08838834764831845f : 0.125f;
 #pragma unroll
     for (int j = 0; j < P; ++j) rr[j] *= inv_sqrt_d;
-    return real;
   };
-  // pass 1: the largest |q|, |q'| of the block fixes a power-of-two fragment scale 2^k with
+  constexpr int NCW = NQ / kW;                 // query columns per warp
+  float qv[NCW][P], qr[NCW][P];
+#pragma unroll
+  for (int k = 0; k < NCW; ++k) prep_column(warp + k * kW, qv[k], qr[k]);
+  {
+    uint32_t* z32 = reinterpret_cast<uint32_t*>(smem + lay.qf);
+    const int nz = (lay.cnt - lay.qf) / 4;
+    for (int i = threadIdx.x; i < nz; i += blockDim.x) z32[i] = 0u;
+  }
+  __syncthreads();
+  // the largest |q|, |q'| of the block fixes a power-of-two fragment scale 2^k with
   // max |fragment| <= 2^14, so the low parts of the split stay normal fp16 (they meet the
   // subnormal code operands of the score MMAs)
   {
     float mx = 0.f;
-    for (int n = warp; n < NQ; n += kW) {
-      float v[P], rr[P];
-      prep_column(n, v, rr);
 #pragma unroll
-      for (int j = 0; j < P; ++j) mx = fmaxf(mx, fmaxf(fabsf(v[j]), fabsf(rr[j])));
-    }
+    for (int k = 0; k < NCW; ++k)
+#pragma unroll
+      for (int j = 0; j < P; ++j) mx = fmaxf(mx, fmaxf(fabsf(qv[k][j]), fabsf(qr[k][j])));
     mx = warp_max(mx);
     if (lane == 0) atomicMax(reinterpret_cast<unsigned*>(red), __float_as_uint(mx));
   }
@@ -316,11 +338,13 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
   const float qscale = ldexpf(1.f, qexp);
   const float code_unit = ldexpf(1.f, 24 - qexp);   // undoes 2^-24 codes and the q scale
   const float inv_code_unit = ldexpf(1.f, qexp - 24);
-  // pass 2: fragments and group sums (the sums in units of code_unit, which scales the score
-  // once at the end)
-  for (int n = warp; n < NQ; n += kW) {
-    float v[P], rr[P];
-    prep_column(n, v, rr);
+  // fragments and group sums (the sums in units of code_unit, which scales the score once at
+  // the end)
+#pragma unroll
+  for (int k = 0; k < NCW; ++k) {
+    const int n = warp + k * kW;
+    const float (&v)[P] = qv[k];
+    const float (&rr)[P] = qr[k];
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int j = 0; j < P; ++j) {
@@ -362,6 +386,7 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
       }
     }
   }
+  __syncthreads();   // fragments and sums visible to every warp
 
   // columns of this lane: score/value-accumulator fragments hold columns 2c and 2c + 1, the
   // value B operand column r
@@ -370,10 +395,10 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
   for (int e = 0; e < 2; ++e) {
     riD[e] = col_ri(2 * c + e);
     const int rc = riD[e] < 0 ? 0 : riD[e];
-    krmD[e] = pick_int(a.off_krm, rc);
-    kaD[e] = pick_int(a.off_ka, rc);
-    vaD[e] = pick_int(a.off_va, rc);
-    vrmD[e] = pick_int(a.off_vrm, rc);
+    krmD[e] = FIXED ? F_RES + rc * F_RS + F_KRM : pick_int(a.off_krm, rc);
+    kaD[e] = FIXED ? F_RES + rc * F_RS + F_KA : pick_int(a.off_ka, rc);
+    vaD[e] = FIXED ? F_RES + rc * F_RS + F_VA : pick_int(a.off_va, rc);
+    vrmD[e] = FIXED ? F_RES + rc * F_RS + F_VRM : pick_int(a.off_vrm, rc);
   }
   const int riB = col_ri(r);
   // loop_mask[e][ri]: all ones where column 2c + e belongs to residual loop ri
@@ -407,10 +432,11 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
       failed = true;
       break;
     }
-    const uint8_t* sb = smem + st * a.stage_bytes;
+    const uint8_t* sb = smem + st * SB;
     const int t0 = t_begin + i * kT;
     if (t0 + 16 * warp < t_end) {   // the warp has tokens in this tile
       const bool v0 = t0 + tr0 < t_end, v1 = t0 + tr1 < t_end;
+      const bool partial = t0 + 16 * warp + 16 > t_end;   // the warp's rows run past the context
 
       // ---------------------------------------------------------------- scores
       float sc[4];
@@ -419,11 +445,11 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
 #pragma unroll
         for (int k = 0; k < 4; ++k) R[k] = E[k] = 0.f;
         uint32_t km0[NG], km1[NG], kw0[NG], kw1[NG];
-        load_words<NG>(sb + a.off_km + tr0 * NG * 4, km0);
-        load_words<NG>(sb + a.off_km + tr1 * NG * 4, km1);
+        load_words<NG>(sb + o_km + tr0 * NG * 4, km0);
+        load_words<NG>(sb + o_km + tr1 * NG * 4, km1);
         // this lane's word of every group (K rows are group-interleaved: one load)
-        load_words<NG>(sb + a.off_kc + tr0 * RB4 + c * NG * 4, kw0);
-        load_words<NG>(sb + a.off_kc + tr1 * RB4 + c * NG * 4, kw1);
+        load_words<NG>(sb + o_kc + tr0 * RB4 + c * NG * 4, kw0);
+        load_words<NG>(sb + o_kc + tr1 * RB4 + c * NG * 4, kw1);
 #pragma unroll
         for (int gq = 0; gq < NG; ++gq) {
           {  // reference
@@ -447,26 +473,19 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
           if (nr > 0) {  // residuals of every loop of the block
             float dsel[4];
             if constexpr (PER_LOOP) {
-              const uint4 q2s0 = QR2[(gq * 2 + 0) * 32 + lane];
-              const uint4 q2s1 = QR2[(gq * 2 + 1) * 32 + lane];
-              uint4 q4s0 = make_uint4(0u, 0u, 0u, 0u), q4s1 = q4s0;
-              if (RES4) {
-                q4s0 = QR4[(gq * 2 + 0) * 32 + lane];
-                q4s1 = QR4[(gq * 2 + 1) * 32 + lane];
-              }
-              float Dr[PER_LOOP ? NRT : 1][4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dsel[k] = 0.f;
 #pragma unroll
               for (int ri = 0; ri < NRT; ++ri) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) Dr[ri][k] = 0.f;
+                float Dr[4] = {0.f, 0.f, 0.f, 0.f};
                 const bool two = !RES4 || a.rbits[ri] == 2;   // without 4-bit loops: all 2-bit
                 uint32_t wl, wh;
                 if (two) {
-                  const int off = a.off_krc[ri] + ((c >> 1) * NG + gq) * 4;
+                  const int off = o_krc(ri) + ((c >> 1) * NG + gq) * 4;
                   wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
                   wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
                 } else {
-                  const int off = a.off_krc[ri] + (c * NG + gq) * 4;
+                  const int off = o_krc(ri) + (c * NG + gq) * 4;
                   wl = lds32(sb + off + tr0 * RB4);
                   wh = lds32(sb + off + tr1 * RB4);
                 }
@@ -480,18 +499,14 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
                     a_pairs_4bit(wl, s, a0, a2);
                     a_pairs_4bit(wh, s, a1, a3);
                   }
-                  const uint4 bq = (RES4 && !two) ? (s ? q4s1 : q4s0) : (s ? q2s1 : q2s0);
-                  mma_f16(Dr[ri], a0, a1, a2, a3, bq.x, bq.y);
-                  mma_f16(Dr[ri], a0, a1, a2, a3, bq.z, bq.w);
+                  const int fi = (gq * 2 + s) * 32 + lane;
+                  const uint4 bq = (RES4 && !two) ? QR4[fi] : QR2[fi];
+                  mma_f16(Dr, a0, a1, a2, a3, bq.x, bq.y);
+                  mma_f16(Dr, a0, a1, a2, a3, bq.z, bq.w);
                 }
-              }
-              // each column keeps its own loop's product
+                // each column keeps its own loop's product
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                float d = Dr[0][k];
-#pragma unroll
-                for (int ri = 1; ri < NRT; ++ri) d = blend(loop_mask[k & 1][ri], Dr[ri][k], d);
-                dsel[k] = d;
+                for (int k = 0; k < 4; ++k) dsel[k] = blend(loop_mask[k & 1][ri], Dr[k], dsel[k]);
               }
             } else {
               // run-time loop count: one accumulator, query fragments masked to each loop's
@@ -503,11 +518,11 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
                 const bool two = !RES4 || a.rbits[ri] == 2;
                 uint32_t wl, wh;
                 if (two) {
-                  const int off = a.off_krc[ri] + ((c >> 1) * NG + gq) * 4;
+                  const int off = o_krc(ri) + ((c >> 1) * NG + gq) * 4;
                   wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
                   wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
                 } else {
-                  const int off = a.off_krc[ri] + (c * NG + gq) * 4;
+                  const int off = o_krc(ri) + (c * NG + gq) * 4;
                   wl = lds32(sb + off + tr0 * RB4);
                   wh = lds32(sb + off + tr1 * RB4);
                 }
@@ -614,18 +629,27 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
             x0 = riD[e] >= 0 ? y0 : 1.f;
             x1 = riD[e] >= 0 ? y1 : 1.f;
           }
-          pa[e] = v0 ? p[e] * x0 : 0.f;
-          pa[2 + e] = v1 ? p[2 + e] * x1 : 0.f;
-          pe[e] = (v0 && riD[e] >= 0) ? p[e] : 0.f;
-          pe[2 + e] = (v1 && riD[e] >= 0) ? p[2 + e] : 0.f;
+          pa[e] = p[e] * x0;
+          pa[2 + e] = p[2 + e] * x1;
+          pe[e] = riD[e] >= 0 ? p[e] : 0.f;
+          pe[2 + e] = riD[e] >= 0 ? p[2 + e] : 0.f;
         }
         uint32_t vm0[NG], vm1[NG];
-        load_words<NG>(sb + a.off_vm + tr0 * NG * 4, vm0);
-        load_words<NG>(sb + a.off_vm + tr1 * NG * 4, vm1);
+        load_words<NG>(sb + o_vm + tr0 * NG * 4, vm0);
+        load_words<NG>(sb + o_vm + tr1 * NG * 4, vm1);
+        if (partial) {   // rows past the context: zero weights and steps whatever the slots hold
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          vm0[g] = v0 ? vm0[g] : 0u;
-          vm1[g] = v1 ? vm1[g] : 0u;
+          for (int e = 0; e < 2; ++e) {
+            pa[e] = v0 ? pa[e] : 0.f;
+            pa[2 + e] = v1 ? pa[2 + e] : 0.f;
+            pe[e] = v0 ? pe[e] : 0.f;
+            pe[2 + e] = v1 ? pe[2 + e] : 0.f;
+          }
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            vm0[g] = v0 ? vm0[g] : 0u;
+            vm1[g] = v1 ? vm1[g] : 0u;
+          }
         }
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
@@ -634,8 +658,8 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
           offR[g][1] = fmaf(pa[1], m0.y, fmaf(pa[3], m1.y, offR[g][1]));
           uint32_t bh0, bh1, bl0, bl1;
           weights_to_b(pa[0] * m0.x, pa[1] * m0.x, pa[2] * m1.x, pa[3] * m1.x, bh0, bh1, bl0, bl1);
-          const uint32_t W0 = lds32(sb + a.off_vc + p0 * D + ((8 * g + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
-          const uint32_t W1 = lds32(sb + a.off_vc + p1 * D + ((8 * g + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
+          const uint32_t W0 = lds32(sb + o_vc + p0 * D + ((8 * g + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
+          const uint32_t W1 = lds32(sb + o_vc + p1 * D + ((8 * g + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
 #pragma unroll
           for (int mtg = 0; mtg < 2; ++mtg) {
             uint32_t x0, x1, x2, x3;
@@ -652,10 +676,12 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
           for (int e = 0; e < 2; ++e) {
             load_words<NG>(sb + vrmD[e] + tr0 * NG * 4, rm0[e]);
             load_words<NG>(sb + vrmD[e] + tr1 * NG * 4, rm1[e]);
+            if (partial) {
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
-              rm0[e][g] = v0 ? rm0[e][g] : 0u;
-              rm1[e][g] = v1 ? rm1[e][g] : 0u;
+              for (int g = 0; g < NG; ++g) {
+                rm0[e][g] = v0 ? rm0[e][g] : 0u;
+                rm1[e][g] = v1 ? rm1[e][g] : 0u;
+              }
             }
           }
 #pragma unroll
@@ -681,9 +707,9 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
                 const int sh = 8 * (r & 1);
                 const int u = 4 * g + (r >> 1);
                 const uint32_t W0 =
-                    lds32(sb + a.off_vrc[ri] + p0 * (2 * RB2) + (u ^ v_unit_swizzle(p0, D / 8)) * 4) >> sh;
+                    lds32(sb + o_vrc(ri) + p0 * (2 * RB2) + (u ^ v_unit_swizzle(p0, D / 8)) * 4) >> sh;
                 const uint32_t W1 =
-                    lds32(sb + a.off_vrc[ri] + p1 * (2 * RB2) + (u ^ v_unit_swizzle(p1, D / 8)) * 4) >> sh;
+                    lds32(sb + o_vrc(ri) + p1 * (2 * RB2) + (u ^ v_unit_swizzle(p1, D / 8)) * 4) >> sh;
 #pragma unroll
                 for (int mtg = 0; mtg < 2; ++mtg) {
                   uint32_t x0, x1, x2, x3;
@@ -694,9 +720,9 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
                 }
               } else if (RES4) {
                 const uint32_t W0 =
-                    lds32(sb + a.off_vrc[ri] + p0 * D + ((8 * g + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
+                    lds32(sb + o_vrc(ri) + p0 * D + ((8 * g + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
                 const uint32_t W1 =
-                    lds32(sb + a.off_vrc[ri] + p1 * D + ((8 * g + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
+                    lds32(sb + o_vrc(ri) + p1 * D + ((8 * g + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
 #pragma unroll
                 for (int mtg = 0; mtg < 2; ++mtg) {
                   uint32_t x0, x1, x2, x3;
@@ -777,30 +803,34 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
     red[kW * NQ + warp * NQ + 2 * c] = lsum[0] * f[0];
     red[kW * NQ + warp * NQ + 2 * c + 1] = lsum[1] * f[1];
   }
-  // this warp's rescaled partial accumulators: buf[warp][column][acc_ref D | acc_res D]
+  // this warp's rescaled partial accumulators: buf[warp][column][acc_ref D | acc_res D], rows
+  // padded by 4 floats so that the float4 stores of a quarter-warp hit distinct banks (query
+  // columns of the block only)
+  constexpr int BS = 2 * D + 4;
   float* buf = reinterpret_cast<float*>(smem);
-  // channels of this thread: 32 g + 4 r + 2 mtg + hh; columns 2c + e
 #pragma unroll
-  for (int g = 0; g < NG; ++g)
+  for (int e = 0; e < 2; ++e) {
+    const int n = 2 * c + e;
+    if (!(n / blk.gw < blk.nl && blk.gi0 + n % blk.gw < a.g)) continue;
+    float* o = buf + (warp * NQ + n) * BS;
+    // channels 32 g + 4 r + j of column n, j = 2 mtg + hh (hh: fragment row r or r + 8)
 #pragma unroll
-    for (int mtg = 0; mtg < 2; ++mtg)
+    for (int g = 0; g < NG; ++g) {
+      float vr[4], ve[4];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {          // hh: row r (j even) or row r+8 (j odd)
-        const int j = 2 * mtg + hh;
-        const int ch = 32 * g + 4 * r + j;
+      for (int j = 0; j < 4; ++j) {
+        const int mtg = j >> 1, hh = j & 1, k = 2 * hh + e;
         const float sc4 = hh ? 0.0625f : 1.f;     // value codes are normal fp16
         const float sc2 = 1.f / float(1 << (2 * j));
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int k = 2 * hh + e;
-          const float vr = fmaf(accR[2 * g + mtg][k], sc4, offR[g][e]);
-          float ve = fmaf(accE2[2 * g + mtg][k], sc2, offE[g][e]);
-          if (RES4) ve = fmaf(accE4[RES4 ? 2 * g + mtg : 0][k], sc4, ve);
-          float* o = buf + (warp * NQ + 2 * c + e) * (2 * D);
-          o[ch] = vr * f[e];
-          o[D + ch] = ve * f[e];
-        }
+        vr[j] = fmaf(accR[2 * g + mtg][k], sc4, offR[g][e]) * f[e];
+        float x = fmaf(accE2[2 * g + mtg][k], sc2, offE[g][e]);
+        if (RES4) x = fmaf(accE4[RES4 ? 2 * g + mtg : 0][k], sc4, x);
+        ve[j] = x * f[e];
       }
+      *reinterpret_cast<float4*>(o + 32 * g + 4 * r) = make_float4(vr[0], vr[1], vr[2], vr[3]);
+      *reinterpret_cast<float4*>(o + D + 32 * g + 4 * r) = make_float4(ve[0], ve[1], ve[2], ve[3]);
+    }
+  }
   __syncthreads();
   const int rec = int(partial_floats_d(D));
   auto rec_ptr = [&](int col) -> float* {
@@ -822,14 +852,21 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
       o[1] = ls;
     }
   }
-  for (int idx = threadIdx.x; idx < NQ * 2 * D; idx += kW * 32) {
-    const int col = idx / (2 * D), k = idx % (2 * D);
+  // records: m, l, 2 pad, acc_ref, acc_res (16-byte aligned)
+  for (int idx = threadIdx.x; idx < NQ * (D / 2); idx += kW * 32) {
+    const int col = idx / (D / 2), q4 = idx % (D / 2);
     float* o = rec_ptr(col);
     if (!o) continue;
-    float v = 0.f;
+    float4 v = *reinterpret_cast<const float4*>(buf + col * BS + 4 * q4);
 #pragma unroll
-    for (int w = 0; w < kW; ++w) v += buf[(w * NQ + col) * (2 * D) + k];
-    o[4 + k] = v;
+    for (int w = 1; w < kW; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(buf + (w * NQ + col) * BS + 4 * q4);
+      v.x += x.x;
+      v.y += x.y;
+      v.z += x.z;
+      v.w += x.w;
+    }
+    *reinterpret_cast<float4*>(o + 4 + 4 * q4) = v;
   }
 }
 

@@ -27,7 +27,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, 
   const int NG = D / 32, NQ = 8, W = 4;
   SmemLayout s;
   int o = stages * stage_bytes;
-  const int merge = W * NQ * 2 * D * 4;
+  const int merge = W * NQ * (2 * D + 4) * 4;
   if (o < merge) o = merge;
   o = (o + 15) & ~15;
   const int frag = NG * 2 * 32 * 16;   // hi and lo f16x2 pairs per lane
