@@ -35,7 +35,7 @@ KERNEL_SOURCES = ("looped_transformer_kv_gb300/csrc/rq_decode_mma.cu",
                   "looped_transformer_kv_gb300/csrc/rq_common.cuh",
                   "looped_transformer_kv_gb300/csrc/rq_kernels.h")
 TRAFFIC = {
-    ("e30902e80e37a98e", "layer_1p4b"): 482835968 + 7121664,   # profiles/rq_mma_kernel_layer_1p4b.md
+    ("a20cf97e42d31401", "layer_1p4b"): 484052736 + 13730048,  # profiles/rq_mma_kernel_layer_1p4b.md
 }
 
 
