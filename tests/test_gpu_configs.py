@@ -42,17 +42,22 @@ def test_full_size_sampled_slices(name):
     rng = np.random.default_rng(17)
     samples = {(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))}
     band = codes = followed = elements = 0
+    worst = {"max_excess": 0.0, "mean_excess": 0.0, "max_abs": 0.0, "mean_abs": 0.0}
     for b, h in sorted(samples):
         st = check_slice(w, b, h, calls, outs)
         band += st["band"]
         codes += st["codes"]
         followed += st["followed"]
         elements += st["elements"]
+        for k in worst:
+            worst[k] = max(worst[k], st[k])
     # elements excused by the near-boundary rule (the GPU's neighbouring choice, within 1e-6
     # of the boundary) stay under 1e-5 of all elements; `band` (codes within the band,
     # exact half-way ties included, which both sides round to even) is reported only
-    print("%s: codes %d, in band %d, elements %d, neighbouring choices taken %d"
-          % (name, codes, band, elements, followed))
+    print("%s: codes %d, in band %d, elements %d, neighbouring choices taken %d; output error "
+          "(worst slice) max excess %.3g, mean excess %.3g, max abs %.3g, mean abs %.3g"
+          % (name, codes, band, elements, followed, worst["max_excess"], worst["mean_excess"],
+             worst["max_abs"], worst["mean_abs"]))
     assert followed < 1e-5 * elements, (followed, elements)
     del w
     torch.cuda.empty_cache()
