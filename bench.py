@@ -321,6 +321,19 @@ def gpu_arm(args, cfg):
                 w.decode_bf16(l, 1, out1[l], ws1)
 
         t_bf_per = timeit(graph_of(bf_per), iters)
+    # the same tokens in a paged cache (64-token pages scattered over a pool with spare pages)
+    t_pg_multi = t_pg_per = None
+    if not args.no_paged:
+        pc, paging, bt = w.paged_twin(spare_pages=64, seed=1)
+        t_pg_multi = timeit(graph_of(lambda: w.decode_paged(pc, paging, 0, L, out, ws)), iters)
+
+        def pg_per():
+            for l in range(L):
+                w.decode_paged(pc, paging, l, 1, out1[l], ws1)
+
+        t_pg_per = timeit(graph_of(pg_per), iters)
+        del pc, paging, bt
+        torch.cuda.empty_cache()
     clk = clocks.stop()
 
     # ---- end to end through the public API with host buffers ----
@@ -386,6 +399,14 @@ def gpu_arm(args, cfg):
         breakdown["speedup_vs_bf16"] = {"multiloop": med(t_bf_multi) / dec_ms,
                                         "perloop": med(t_bf_per) / med(t_per)}
     breakdown["storage_reduction_vs_bf16"] = 1 - (ref_b + sum(res_b)) / (L * 2 * d * 2)
+    if t_pg_multi:
+        for name, tt, nb, base in (("rq_paged_decode_multiloop", t_pg_multi, bytes_multi, dec_ms),
+                                   ("rq_paged_decode_perloop", t_pg_per, bytes_per, med(t_per))):
+            m = med(tt)
+            breakdown[name] = {"ms": m, "kv_tokens_s": kvtok / (m * 1e-3),
+                               "gbs": nb / (m * 1e-3) / 1e9,
+                               "frac_hbm_measured": nb / (m * 1e-3) / 1e9 / hbm,
+                               "time_vs_contiguous": m / base}
 
     value = kvtok * NL * world / (ms * 1e-3)
     line = {
@@ -424,6 +445,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-paged", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -147,6 +147,45 @@ rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k,
                                    const int32_t* ctx_lens, int32_t max_ctx, uint16_t* out,
                                    void* ws, size_t ws_bytes, void* stream);
 
+/* Paged cache (rit.work summary, "When ResidualQuant changes the infrastructure plan": the
+ * pages' integration keeps the serving engine's paged KV cache; this is its block-table
+ * form).  A page holds 64 consecutive tokens of one sequence for every kv-head.  In paged
+ * mode every array of rq_cache except rot_signs is laid out per page instead of per
+ * sequence:
+ *   ref_codes[kv] uint8 [n_pages][Hkv][64][d/2], ref_meta[kv] fp16 [n_pages][Hkv][64][ng][2],
+ *   res_codes[kv][l] uint8 [n_pages][Hkv][64][d*b_l/8], res_meta[kv][l] fp16
+ *   [n_pages][Hkv][64][ng][2], alpha[kv][l] fp16 [n_pages][Hkv][64],
+ * with the same row formats as above (V token pairs and their swizzle follow the token's
+ * position within its page).  Tokens 64j..64j+63 of sequence b live in physical page
+ * block_table[b * max_pages + j].  shape->capacity must equal 64 * max_pages (the logical
+ * capacity of a sequence).  The table is read on the device: an entry outside
+ * [0, n_pages) is never dereferenced -- the encode skips that token, the decode reads page 0
+ * instead and flags the workspace error word (outputs NaN). */
+typedef struct {
+  const int32_t* block_table;  /* device int32 [B][max_pages]                         */
+  int32_t max_pages;           /* table columns: logical pages per sequence            */
+  int32_t n_pages;             /* physical pages in each array                         */
+} rq_paging;
+
+/* Bytes of one layer's paged cache with n_pages physical pages (0 for an invalid shape). */
+size_t rq_paged_cache_bytes(const rq_shape* shape, int32_t n_pages);
+
+/* rq_encode_append on a paged cache: positions are logical token positions of each
+ * sequence (< capacity); the slot is found through the block table. */
+rq_status rq_paged_encode_append(const rq_shape* shape, const rq_cache* cache,
+                                 const rq_paging* paging, const uint16_t* kv_new,
+                                 const int64_t strides[5], const int32_t* positions,
+                                 int32_t pos_begin, int32_t n_new, void* stream);
+
+/* rq_decode_attention on a paged cache (same arguments, same workspace size, same
+ * results bit for bit as on a contiguous cache holding the same tokens). */
+rq_status rq_paged_decode_attention(const rq_shape* shape, const rq_cache* cache,
+                                    const rq_paging* paging, const uint16_t* q,
+                                    int32_t loop_begin, int32_t loop_count,
+                                    const uint16_t* pending_kv, const int32_t* ctx_lens,
+                                    int32_t max_ctx, uint16_t* out, void* ws, size_t ws_bytes,
+                                    void* stream);
+
 /* Decode attention without a caller-provided workspace, for callers that cannot allocate
  * device memory: e.g. a plug-in whose host framework owns every device allocation and hands
  * it only input and output tensors, or a C caller that must not allocate once it has

@@ -15,7 +15,8 @@ STATUS = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_UNSUPPORTED",
 EXPORTS = ("rq_cache_bytes", "rq_encode_append", "rq_decode_workspace_bytes",
            "rq_decode_attention", "rq_bf16_decode_attention", "rq_status_str",
            "rq_synth_states", "rq_synth_queries", "rq_decode_noalloc_scratch_bytes",
-           "rq_decode_attention_noalloc")
+           "rq_decode_attention_noalloc", "rq_paged_cache_bytes", "rq_paged_encode_append",
+           "rq_paged_decode_attention")
 
 
 class RqShape(ctypes.Structure):
@@ -33,6 +34,10 @@ class RqCache(ctypes.Structure):
     _fields_ = [("ref_codes", _P * 2), ("ref_meta", _P * 2),
                 ("res_codes", (_P * RQ_MAX_LOOPS) * 2), ("res_meta", (_P * RQ_MAX_LOOPS) * 2),
                 ("alpha", (_P * RQ_MAX_LOOPS) * 2), ("rot_signs", _P * 2)]
+
+
+class RqPaging(ctypes.Structure):
+    _fields_ = [("block_table", _P), ("max_pages", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
 
 
 class RqSynthParams(ctypes.Structure):
@@ -77,6 +82,13 @@ def lib():
     L.rq_decode_noalloc_scratch_bytes.restype = sz
     L.rq_decode_attention_noalloc.argtypes = [S, C, _P, i32, i32, _P, _P, i32, _P, _P]
     L.rq_decode_attention_noalloc.restype = i32
+    G = ctypes.POINTER(RqPaging)
+    L.rq_paged_cache_bytes.argtypes = [S, i32]
+    L.rq_paged_cache_bytes.restype = sz
+    L.rq_paged_encode_append.argtypes = [S, C, G, _P, ctypes.POINTER(i64), _P, i32, i32, _P]
+    L.rq_paged_encode_append.restype = i32
+    L.rq_paged_decode_attention.argtypes = [S, C, G, _P, i32, i32, _P, _P, i32, _P, _P, sz, _P]
+    L.rq_paged_decode_attention.restype = i32
     L.rq_status_str.argtypes = [i32]
     L.rq_status_str.restype = ctypes.c_char_p
     P = ctypes.POINTER(RqSynthParams)

@@ -53,24 +53,30 @@ rq_status check_decode(const rq_shape* s, const uint16_t* q, int32_t loop_begin,
 
 rq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RQ_OK : RQ_ERR_CUDA; }
 
-}  // namespace
+rq_status check_paging(const rq_shape* s, const rq_paging* pg) {
+  if (!pg || !pg->block_table || pg->max_pages <= 0 || pg->n_pages <= 0)
+    return RQ_ERR_INVALID_ARG;
+  if (int64_t(s->capacity) != int64_t(64) * pg->max_pages) return RQ_ERR_INVALID_ARG;
+  if (int64_t(pg->n_pages) * s->n_kv_heads * 64 > (int64_t(1) << 40)) return RQ_ERR_UNSUPPORTED;
+  return RQ_OK;
+}
 
-extern "C" {
-
-size_t rq_cache_bytes(const rq_shape* s) {
-  if (check_shape(s) != RQ_OK) return 0;
+// Bytes of one token of one kv-head, K and V, every array of the packed cache.
+size_t token_head_bytes(const rq_shape* s) {
   const size_t d = size_t(s->head_dim), ng = d / 32;
   size_t per = d / 2 + 4 * ng;
   for (int l = 0; l < s->n_loops - 1; ++l) per += d * size_t(s->res_bits[l]) / 8 + 4 * ng + 2;
-  return 2 * per * size_t(s->capacity) * size_t(s->n_kv_heads) * size_t(s->batch);
+  return 2 * per;
 }
 
-rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache, const uint16_t* kv_new,
-                           const int64_t strides[5], const int32_t* positions, int32_t pos_begin,
-                           int32_t n_new, void* stream) {
+rq_status encode_common(const rq_shape* shape, const rq_cache* cache, const rq_paging* paging,
+                        const uint16_t* kv_new, const int64_t strides[5],
+                        const int32_t* positions, int32_t pos_begin, int32_t n_new,
+                        void* stream) {
   rq_status st = check_shape(shape);
   if (st != RQ_OK) return st;
   if ((st = check_cache(shape, cache)) != RQ_OK) return st;
+  if (paging && (st = check_paging(shape, paging)) != RQ_OK) return st;
   if (!kv_new || !strides || n_new < 0) return RQ_ERR_INVALID_ARG;
   for (int k = 0; k < 5; ++k)
     if (strides[k] < 0) return RQ_ERR_INVALID_ARG;
@@ -78,11 +84,62 @@ rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache, const u
     return RQ_ERR_INVALID_ARG;
   if (n_new == 0) return RQ_OK;
   try {
-    return from_cuda(rq::launch_encode(*shape, *cache, kv_new, strides, positions, pos_begin,
-                                       n_new, static_cast<cudaStream_t>(stream)));
+    return from_cuda(rq::launch_encode(*shape, *cache, paging, kv_new, strides, positions,
+                                       pos_begin, n_new, static_cast<cudaStream_t>(stream)));
   } catch (...) {
     return RQ_ERR_INTERNAL;
   }
+}
+
+rq_status decode_common(const rq_shape* shape, const rq_cache* cache, const rq_paging* paging,
+                        const uint16_t* q, int32_t loop_begin, int32_t loop_count,
+                        const uint16_t* pending_kv, const int32_t* ctx_lens, int32_t max_ctx,
+                        uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  rq_status st = check_shape(shape);
+  if (st != RQ_OK) return st;
+  if ((st = check_cache(shape, cache)) != RQ_OK) return st;
+  if (paging && (st = check_paging(shape, paging)) != RQ_OK) return st;
+  if ((st = check_decode(shape, q, loop_begin, loop_count, ctx_lens, max_ctx, out, ws,
+                         ws_bytes)) != RQ_OK)
+    return st;
+  try {
+    return from_cuda(rq::launch_rq_decode(*shape, *cache, paging, q, loop_begin, loop_count,
+                                          pending_kv, ctx_lens, max_ctx, out,
+                                          static_cast<float*>(ws),
+                                          static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return RQ_ERR_INTERNAL;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rq_cache_bytes(const rq_shape* s) {
+  if (check_shape(s) != RQ_OK) return 0;
+  return token_head_bytes(s) * size_t(s->capacity) * size_t(s->n_kv_heads) * size_t(s->batch);
+}
+
+size_t rq_paged_cache_bytes(const rq_shape* s, int32_t n_pages) {
+  if (check_shape(s) != RQ_OK || n_pages <= 0) return 0;
+  return token_head_bytes(s) * 64 * size_t(n_pages) * size_t(s->n_kv_heads);
+}
+
+rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache, const uint16_t* kv_new,
+                           const int64_t strides[5], const int32_t* positions, int32_t pos_begin,
+                           int32_t n_new, void* stream) {
+  return encode_common(shape, cache, nullptr, kv_new, strides, positions, pos_begin, n_new,
+                       stream);
+}
+
+rq_status rq_paged_encode_append(const rq_shape* shape, const rq_cache* cache,
+                                 const rq_paging* paging, const uint16_t* kv_new,
+                                 const int64_t strides[5], const int32_t* positions,
+                                 int32_t pos_begin, int32_t n_new, void* stream) {
+  if (!paging) return RQ_ERR_INVALID_ARG;
+  return encode_common(shape, cache, paging, kv_new, strides, positions, pos_begin, n_new,
+                       stream);
 }
 
 size_t rq_decode_workspace_bytes(const rq_shape* s, int32_t loop_count, int32_t max_ctx) {
@@ -97,19 +154,19 @@ rq_status rq_decode_attention(const rq_shape* shape, const rq_cache* cache, cons
                               int32_t loop_begin, int32_t loop_count, const uint16_t* pending_kv,
                               const int32_t* ctx_lens, int32_t max_ctx, uint16_t* out, void* ws,
                               size_t ws_bytes, void* stream) {
-  rq_status st = check_shape(shape);
-  if (st != RQ_OK) return st;
-  if ((st = check_cache(shape, cache)) != RQ_OK) return st;
-  if ((st = check_decode(shape, q, loop_begin, loop_count, ctx_lens, max_ctx, out, ws,
-                         ws_bytes)) != RQ_OK)
-    return st;
-  try {
-    return from_cuda(rq::launch_rq_decode(*shape, *cache, q, loop_begin, loop_count, pending_kv,
-                                          ctx_lens, max_ctx, out, static_cast<float*>(ws),
-                                          static_cast<cudaStream_t>(stream)));
-  } catch (...) {
-    return RQ_ERR_INTERNAL;
-  }
+  return decode_common(shape, cache, nullptr, q, loop_begin, loop_count, pending_kv, ctx_lens,
+                       max_ctx, out, ws, ws_bytes, stream);
+}
+
+rq_status rq_paged_decode_attention(const rq_shape* shape, const rq_cache* cache,
+                                    const rq_paging* paging, const uint16_t* q,
+                                    int32_t loop_begin, int32_t loop_count,
+                                    const uint16_t* pending_kv, const int32_t* ctx_lens,
+                                    int32_t max_ctx, uint16_t* out, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  if (!paging) return RQ_ERR_INVALID_ARG;
+  return decode_common(shape, cache, paging, q, loop_begin, loop_count, pending_kv, ctx_lens,
+                       max_ctx, out, ws, ws_bytes, stream);
 }
 
 rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k, const uint16_t* v,

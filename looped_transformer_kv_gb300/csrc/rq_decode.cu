@@ -142,7 +142,8 @@ SplitPlan plan_splits(const rq_shape& s, int loop_count, int max_ctx) {
 
 size_t partial_floats(const rq_shape& s) { return partial_floats_d(s.head_dim); }
 
-cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const uint16_t* q,
+cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
+                             const uint16_t* q,
                              int loop_begin, int loop_count, const uint16_t* pending,
                              const int32_t* ctx_lens, int max_ctx, uint16_t* out, float* ws,
                              cudaStream_t stream) {
@@ -151,7 +152,7 @@ cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const uin
   float* part = ws + kWsHeaderBytes / sizeof(float);
   cudaError_t e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream);
   if (e != cudaSuccess) return e;
-  e = launch_rq_decode_mma(s, cache, q, loop_begin, loop_count, ctx_lens, plan.n_splits,
+  e = launch_rq_decode_mma(s, cache, paging, q, loop_begin, loop_count, ctx_lens, plan.n_splits,
                            plan.tokens_per_split, part, err, stream);
   if (e != cudaSuccess) return e;
   return launch_combine(s, cache.rot_signs[1], q, loop_count, pending, plan.n_splits, out, part,

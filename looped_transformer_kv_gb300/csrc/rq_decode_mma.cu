@@ -69,6 +69,8 @@ struct MmaArgs {
   QueryBlock blk;
   float scale_log2;
   int n_stages, stage_bytes;
+  const int32_t* bt;   // block table of a paged cache, or null
+  int max_pages, n_pages, n_pg;   // table columns, physical pages, page-id slots in shared memory
   int off_kc, off_km, off_vc, off_vm;
   int off_krc[kMaxResPerBlock], off_krm[kMaxResPerBlock], off_ka[kMaxResPerBlock];
   int off_vrc[kMaxResPerBlock], off_vrm[kMaxResPerBlock], off_va[kMaxResPerBlock];
@@ -180,7 +182,8 @@ __device__ __forceinline__ void weights_to_b(float w00, float w01, float w10, fl
 }
 
 // NRT >= 0: the block's number of residual loops, fixed at compile time; -1: read at run time.
-template <int D, bool RES4, int NRT>
+// PAGED: tiles are found through the block table of a paged cache.
+template <int D, bool RES4, int NRT, bool PAGED>
 __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NG = D / 32;
   constexpr int NQ = kNQ;
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
     if (threadIdx.x == 0) atomicOr(a.err, 1u);
     return;
   }
-  const SmemLayout lay = smem_layout(D, RES4, a.n_stages, SB);
+  const SmemLayout lay = smem_layout(D, RES4, a.n_stages, SB, a.n_pg);
   uint4* QF = reinterpret_cast<uint4*>(smem + lay.qf);
   uint4* QR2 = reinterpret_cast<uint4*>(smem + lay.qr2);
   uint4* QR4 = reinterpret_cast<uint4*>(smem + lay.qr4);
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
   float* red = reinterpret_cast<float*>(smem + lay.red);      // [2][kW][NQ]
   unsigned* cnt = reinterpret_cast<unsigned*>(smem + lay.cnt);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
+  int* pid = reinterpret_cast<int*>(smem + lay.pg);   // physical page of each tile (paged)
 
   // residual index (into the block's residual loops) of query column n, -1 if the column
   // is the final loop's or a padding column
@@ -244,6 +248,17 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
   const int ntiles = t_end > t_begin ? (t_end - t_begin + kT - 1) / kT : 0;
   const int64_t slot = int64_t(b) * a.H + h;
   const int S = a.n_stages;
+  constexpr bool paged = PAGED;
+  // physical page of the split's tile (a paged cache's tiles are its 64-token pages); a
+  // table entry out of range is never dereferenced: page 0 is read and the call flagged
+  auto page_of = [&](int tile) -> int {
+    int pg = a.bt[int64_t(b) * a.max_pages + t_begin / kT + tile];
+    if (pg < 0 || pg >= a.n_pages) {
+      atomicOr(a.err, 1u);
+      pg = 0;
+    }
+    return pg;
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
@@ -256,7 +271,8 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
     const int st = tile % S;
     const uint32_t bar = smem_u32(&bars[st]);
     const uint32_t dst = smem_u32(smem + st * a.stage_bytes);
-    const int64_t tok = slot * a.cap + t_begin + int64_t(tile) * kT;
+    const int64_t tok = paged ? (int64_t(pid[tile]) * a.H + h) * kT
+                              : slot * a.cap + t_begin + int64_t(tile) * kT;
     mbar_arrive_expect_tx(bar, uint32_t(a.stage_bytes));
     bulk_g2s(dst + a.off_kc, a.kc + tok * RB4, kT * RB4, bar);
     bulk_g2s(dst + a.off_km, a.km + tok * NG * 2, kT * NG * 4, bar);
@@ -276,6 +292,8 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
   };
   if (threadIdx.x == 0) {   // the barriers' initialisation is ordered before by the fence
     const int n0 = S < ntiles ? S : ntiles;
+    if (paged)
+      for (int i = 0; i < n0; ++i) pid[i] = page_of(i);
     for (int i = 0; i < n0; ++i) issue(i);
     cnt[kIssuedSlot] = unsigned(n0);
   }
@@ -313,6 +331,8 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
     uint32_t* z32 = reinterpret_cast<uint32_t*>(smem + lay.qf);
     const int nz = (lay.cnt - lay.qf) / 4;
     for (int i = threadIdx.x; i < nz; i += blockDim.x) z32[i] = 0u;
+    if (paged)   // the pages of the later tiles, read before the first refill needs them
+      for (int i = S + threadIdx.x; i < ntiles; i += blockDim.x) pid[i] = page_of(i);
   }
   __syncthreads();
   // the largest |q|, |q'| of the block fixes a power-of-two fragment scale 2^k with
@@ -872,31 +892,36 @@ __global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constan
 
 using KernelFn = void (*)(MmaArgs);
 
-template <int D>
+template <int D, bool PG>
 KernelFn pick_generic(bool res4) {
-  return res4 ? rq_mma_kernel<D, true, -1> : rq_mma_kernel<D, false, -1>;
+  return res4 ? rq_mma_kernel<D, true, -1, PG> : rq_mma_kernel<D, false, -1, PG>;
 }
 
 // Variants with the residual-loop count fixed at compile time, for the common blocks: one
 // loop of a per-loop call (0 or 1 residual), two loops of a 4-query-head GQA block (2) and
-// all four loops of a 4-loop model (3).
-KernelFn pick(int D, bool res4, int nr) {
+// all four loops of a 4-loop model (3); each for a contiguous and for a paged cache.
+template <bool PG>
+KernelFn pick_pg(int D, bool res4, int nr) {
   if (D == 128 && !res4) {
-    if (nr == 0) return rq_mma_kernel<128, false, 0>;
-    if (nr == 1) return rq_mma_kernel<128, false, 1>;
-    if (nr == 2) return rq_mma_kernel<128, false, 2>;
-    if (nr == 3) return rq_mma_kernel<128, false, 3>;
+    if (nr == 0) return rq_mma_kernel<128, false, 0, PG>;
+    if (nr == 1) return rq_mma_kernel<128, false, 1, PG>;
+    if (nr == 2) return rq_mma_kernel<128, false, 2, PG>;
+    if (nr == 3) return rq_mma_kernel<128, false, 3, PG>;
   }
   if (D == 128 && res4) {
-    if (nr == 1) return rq_mma_kernel<128, true, 1>;
-    if (nr == 3) return rq_mma_kernel<128, true, 3>;
+    if (nr == 1) return rq_mma_kernel<128, true, 1, PG>;
+    if (nr == 3) return rq_mma_kernel<128, true, 3, PG>;
   }
   if (D == 64 && !res4) {
-    if (nr == 0) return rq_mma_kernel<64, false, 0>;
-    if (nr == 1) return rq_mma_kernel<64, false, 1>;
-    if (nr == 3) return rq_mma_kernel<64, false, 3>;
+    if (nr == 0) return rq_mma_kernel<64, false, 0, PG>;
+    if (nr == 1) return rq_mma_kernel<64, false, 1, PG>;
+    if (nr == 3) return rq_mma_kernel<64, false, 3, PG>;
   }
-  return D == 128 ? pick_generic<128>(res4) : pick_generic<64>(res4);
+  return D == 128 ? pick_generic<128, PG>(res4) : pick_generic<64, PG>(res4);
+}
+
+KernelFn pick(int D, bool res4, int nr, bool paged) {
+  return paged ? pick_pg<true>(D, res4, nr) : pick_pg<false>(D, res4, nr);
 }
 
 // Opt every kernel variant in to the largest dynamic shared memory, once per device.
@@ -909,12 +934,13 @@ cudaError_t prepare_kernels() {
     err[dev] = cudaSuccess;
     for (int D : {64, 128})
       for (bool r4 : {false, true})
-        for (int nr = -1; nr <= kMaxResPerBlock; ++nr) {
-          cudaError_t e = cudaFuncSetAttribute(pick(D, r4, nr),
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               200 * 1024);
-          if (e != cudaSuccess) err[dev] = e;
-        }
+        for (bool pg : {false, true})
+          for (int nr = -1; nr <= kMaxResPerBlock; ++nr) {
+            cudaError_t e = cudaFuncSetAttribute(pick(D, r4, nr, pg),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 200 * 1024);
+            if (e != cudaSuccess) err[dev] = e;
+          }
   });
   return err[dev];
 }
@@ -923,7 +949,7 @@ cudaError_t prepare_kernels() {
 int resident_ctas(int D, bool res4, int nr, size_t smem) {
   int n = 0;
   if (prepare_kernels() == cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, res4, nr), kW * 32, smem) ==
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, res4, nr, false), kW * 32, smem) ==
           cudaSuccess &&
       n > 0)
     return n;
@@ -938,7 +964,8 @@ struct BlockLaunch {
 };
 
 // Arguments, stage layout and shared memory of one query block (no launch).
-bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq, BlockLaunch& bl) {
+bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq, int n_pg,
+                 BlockLaunch& bl) {
   MmaArgs& a = bl.a;
   memset(&a, 0, sizeof(a));
   const int D = s.head_dim, NG = D / 32;
@@ -972,11 +999,12 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
   }
   a.stage_bytes = off;
   a.blk = bq;
+  a.n_pg = n_pg;
   bl.res4 = res4;
   // most resident CTAs per SM first (latency hiding), then the deepest pipeline
   int best_ctas = 0;
   for (int stages = 3; stages >= 2; --stages) {
-    const size_t sm = smem_layout(D, res4, stages, a.stage_bytes).total;
+    const size_t sm = smem_layout(D, res4, stages, a.stage_bytes, n_pg).total;
     if (sm > 200 * 1024) continue;
     const int ctas = resident_ctas(D, res4, bq.nr, sm);
     if (ctas > best_ctas) {
@@ -1035,17 +1063,17 @@ SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int 
   int ctas = 0;
   for (int i = 0; i < nb; ++i) {
     BlockLaunch bl;
-    if (!build_block(s, dummy, blocks[i], bl)) continue;
+    if (!build_block(s, dummy, blocks[i], 0, bl)) continue;
     const int n = resident_ctas(s.head_dim, bl.res4, blocks[i].nr, bl.smem);
     if (ctas == 0 || n < ctas) ctas = n;
   }
   return plan_splits_for(s, max_ctx, ctas > 0 ? ctas : 1, kT);
 }
 
-cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const uint16_t* q,
-                                 int loop_begin, int loop_count, const int32_t* ctx_lens,
-                                 int n_splits, int tokens_per_split, float* part, unsigned* err,
-                                 cudaStream_t stream) {
+cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
+                                 const uint16_t* q, int loop_begin, int loop_count,
+                                 const int32_t* ctx_lens, int n_splits, int tokens_per_split,
+                                 float* part, unsigned* err, cudaStream_t stream) {
   cudaError_t e = prepare_kernels();
   if (e != cudaSuccess) return e;
   QueryBlock blocks[64];
@@ -1055,8 +1083,12 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
   const float scale = s.softmax_scale > 0.f ? s.softmax_scale : 1.0f / sqrtf(float(s.head_dim));
   for (int bi = 0; bi < nb; ++bi) {
     BlockLaunch bl;
-    if (!build_block(s, cache, blocks[bi], bl)) return cudaErrorInvalidConfiguration;
+    const int n_pg = paging ? tokens_per_split / kT : 0;
+    if (!build_block(s, cache, blocks[bi], n_pg, bl)) return cudaErrorInvalidConfiguration;
     MmaArgs& a = bl.a;
+    a.bt = paging ? paging->block_table : nullptr;
+    a.max_pages = paging ? paging->max_pages : 0;
+    a.n_pages = paging ? paging->n_pages : 0;
     a.ksigns = cache.rot_signs[0];
     a.q = q;
     a.ctx_lens = ctx_lens;
@@ -1074,7 +1106,7 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.tokens_per_split = tokens_per_split;
     a.scale_log2 = scale * kLog2e;
     dim3 grid(n_splits, s.n_kv_heads, s.batch);
-    pick(s.head_dim, bl.res4, blocks[bi].nr)<<<grid, kW * 32, bl.smem, stream>>>(a);
+    pick(s.head_dim, bl.res4, blocks[bi].nr, paging != nullptr)<<<grid, kW * 32, bl.smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

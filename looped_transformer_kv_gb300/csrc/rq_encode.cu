@@ -17,6 +17,8 @@ struct EncodeArgs {
   int32_t n_new;
   int32_t B, H, L, cap;
   int8_t res_bits[RQ_MAX_LOOPS];
+  const int32_t* bt;     // block table of a paged cache, or null
+  int32_t max_pages, n_pages;
 };
 
 // Group min / max over the lanes that share a 32-channel group (LPG lanes).
@@ -109,8 +111,19 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
   const int pos = a.positions ? a.positions[int64_t(b) * a.n_new + j] : a.pos_begin + j;
   if (pos < 0 || pos >= a.cap) return;
   const bool is_v = kv == 1;
-  const int64_t slot_tok = int64_t(b) * a.H + h;        // (b, h) slot index
-  const int64_t tok = pos;
+  // token rows of this (sequence, kv-head) start at row `base` of every array; the token is
+  // row base + tok.  Paged: the 64-token page holding the position, through the block table.
+  int64_t base;
+  int64_t tok;
+  if (a.bt) {
+    const int pg = a.bt[int64_t(b) * a.max_pages + (pos >> 6)];
+    if (pg < 0 || pg >= a.n_pages) return;
+    base = (int64_t(pg) * a.H + h) * 64;
+    tok = pos & 63;
+  } else {
+    base = (int64_t(b) * a.H + h) * a.cap;
+    tok = pos;
+  }
 
   const uint16_t* src = a.kv_new + int64_t(b) * a.sb + int64_t(j) * a.st + int64_t(kv) * a.skv +
                         int64_t(h) * a.sh + lane * P;
@@ -128,11 +141,11 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
   uint16_t s_bits, z_bits;
   quantize_lane<P, 15>(x_ref, c, ref_hat, s_bits, z_bits);
   {
-    uint8_t* codes = a.cache.ref_codes[kv] + slot_tok * int64_t(a.cap) * (D / 2);
+    uint8_t* codes = a.cache.ref_codes[kv] + base * (D / 2);
     store_codes<P, 4>(codes, tok, D / 2, is_v, c, lane);
     if (lane % LPG == 0) {
       const int g = lane / LPG;
-      uint16_t* meta = a.cache.ref_meta[kv] + (slot_tok * a.cap + tok) * (2 * NG) + 2 * g;
+      uint16_t* meta = a.cache.ref_meta[kv] + (base + tok) * (2 * NG) + 2 * g;
       *reinterpret_cast<uint32_t*>(meta) = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
     }
   }
@@ -161,7 +174,7 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
     const float alpha = den > 0.f ? __fdiv_rn(num, den) : 0.f;
     const uint16_t a_bits = float_to_half_bits(alpha);
     const float a_h = half_bits_to_float(a_bits);
-    if (lane == 0) a.cache.alpha[kv][l][slot_tok * a.cap + tok] = a_bits;
+    if (lane == 0) a.cache.alpha[kv][l][base + tok] = a_bits;
     // residual, rotation R r = H (signs * r) / sqrt(d)
     float y[P];
 #pragma unroll
@@ -172,7 +185,7 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
     float deq[P];
     const int bits = a.res_bits[l];
     const int row = D * bits / 8;
-    uint8_t* codes = a.cache.res_codes[kv][l] + slot_tok * int64_t(a.cap) * row;
+    uint8_t* codes = a.cache.res_codes[kv][l] + base * row;
     if (bits == 2) {
       quantize_lane<P, 3>(y, c, deq, s_bits, z_bits);
       store_codes<P, 2>(codes, tok, row, is_v, c, lane);
@@ -182,7 +195,7 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
     }
     if (lane % LPG == 0) {
       const int g = lane / LPG;
-      uint16_t* meta = a.cache.res_meta[kv][l] + (slot_tok * a.cap + tok) * (2 * NG) + 2 * g;
+      uint16_t* meta = a.cache.res_meta[kv][l] + (base + tok) * (2 * NG) + 2 * g;
       *reinterpret_cast<uint32_t*>(meta) = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
     }
   }
@@ -190,7 +203,8 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
 
 }  // namespace
 
-cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const uint16_t* kv_new,
+cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
+                          const uint16_t* kv_new,
                           const int64_t strides[5], const int32_t* positions, int32_t pos_begin,
                           int32_t n_new, cudaStream_t stream) {
   EncodeArgs a;
@@ -209,6 +223,9 @@ cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const uint16
   a.L = s.n_loops;
   a.cap = s.capacity;
   for (int l = 0; l < RQ_MAX_LOOPS; ++l) a.res_bits[l] = s.res_bits[l];
+  a.bt = paging ? paging->block_table : nullptr;
+  a.max_pages = paging ? paging->max_pages : 0;
+  a.n_pages = paging ? paging->n_pages : 0;
   const int64_t warps = int64_t(s.batch) * n_new * s.n_kv_heads * 2;
   const int64_t blocks = (warps + 3) / 4;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

@@ -20,10 +20,12 @@ struct QueryBlock {
 // Shared-memory layout of the tensor-core decode kernel (byte offsets).  The stage region
 // also holds the four warps' partial accumulators when the tiles are done.
 struct SmemLayout {
-  int qf, qr2, qr4, qsum, qrsum, red, cnt, bars, total;
+  int qf, qr2, qr4, qsum, qrsum, red, cnt, pg, bars, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, int stage_bytes) {
+// page_ids: physical page ids of a split's tiles kept for a paged cache (0 otherwise).
+__host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, int stage_bytes,
+                                                  int page_ids) {
   const int NG = D / 32, NQ = 8, W = 4;
   SmemLayout s;
   int o = stages * stage_bytes;
@@ -38,6 +40,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, 
   s.qrsum = o; o += NG * NQ * 4;
   s.red = o;   o += 2 * W * NQ * 4;
   s.cnt = o;   o += 16 * 4;           // stage release counters, tiles issued
+  s.pg = o;    o += page_ids * 4;
   o = (o + 7) & ~7;
   s.bars = o;  o += stages * 8;
   s.total = o;
@@ -49,10 +52,10 @@ __host__ __device__ constexpr size_t partial_floats_d(int D) { return size_t(4 +
 
 int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* out, int max_out);
 
-cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const uint16_t* q,
-                                 int loop_begin, int loop_count, const int32_t* ctx_lens,
-                                 int n_splits, int tokens_per_split, float* part, unsigned* err,
-                                 cudaStream_t stream);
+cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
+                                 const uint16_t* q, int loop_begin, int loop_count,
+                                 const int32_t* ctx_lens, int n_splits, int tokens_per_split,
+                                 float* part, unsigned* err, cudaStream_t stream);
 
 struct SplitPlan {
   int n_splits;          // split-KV partitions of the context
@@ -67,11 +70,13 @@ SplitPlan plan_splits_bf16(const rq_shape& s, int max_ctx);
 SplitPlan plan_splits(const rq_shape& s, int loop_count, int max_ctx);
 size_t partial_floats(const rq_shape& s);  // floats of one partial record
 
-cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const uint16_t* kv_new,
+cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
+                          const uint16_t* kv_new,
                           const int64_t strides[5], const int32_t* positions, int32_t pos_begin,
                           int32_t n_new, cudaStream_t stream);
 
-cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const uint16_t* q,
+cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
+                             const uint16_t* q,
                              int loop_begin, int loop_count, const uint16_t* pending,
                              const int32_t* ctx_lens, int max_ctx, uint16_t* out, float* ws,
                              cudaStream_t stream);

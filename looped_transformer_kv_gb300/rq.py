@@ -9,7 +9,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import RQ_MAX_LOOPS, RqCache, RqShape, RqSynthParams, check
+from ._lib import RQ_MAX_LOOPS, RqCache, RqPaging, RqShape, RqSynthParams, check
 
 GROUP = 32
 
@@ -39,11 +39,20 @@ def res_bits_of(shape):
     return [int(shape.res_bits[l]) for l in range(shape.n_loops - 1)]
 
 
-class PackedCache:
-    """Device arrays of one layer's packed cache (layout of include/rq.h) + rotation signs."""
+PAGE = 64   # tokens per page of a paged cache
 
-    def __init__(self, shape, rot_signs, device="cuda"):
+
+class PackedCache:
+    """Device arrays of one layer's packed cache (layout of include/rq.h) + rotation signs.
+
+    With n_pages, the arrays are laid out per 64-token page ([n_pages][Hkv][64][...], the
+    paged form of include/rq.h) instead of per sequence ([B][Hkv][capacity][...])."""
+
+    def __init__(self, shape, rot_signs, device="cuda", n_pages=None):
         B, H, cap, d = shape.batch, shape.n_kv_heads, shape.capacity, shape.head_dim
+        self.n_pages = n_pages
+        if n_pages is not None:
+            B, cap = n_pages, PAGE
         ng = d // GROUP
         u8, f16 = torch.uint8, torch.float16
         self.shape = shape
@@ -82,6 +91,38 @@ class PackedCache:
 
 def cache_bytes(shape):
     return int(_lib.lib().rq_cache_bytes(ctypes.byref(shape)))
+
+
+def paged_cache_bytes(shape, n_pages):
+    return int(_lib.lib().rq_paged_cache_bytes(ctypes.byref(shape), int(n_pages)))
+
+
+def make_paging(block_table, n_pages):
+    """rq_paging for a device int32 block table [B][max_pages] (kept alive by the caller)."""
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2
+    assert block_table.is_contiguous()
+    g = RqPaging()
+    g.block_table = block_table.data_ptr()
+    g.max_pages = block_table.shape[1]
+    g.n_pages = int(n_pages)
+    return g
+
+
+def paged_encode_append(shape, cache, paging, kv_new, positions=None, pos_begin=0, stream=None):
+    """rq_paged_encode_append; kv_new as in encode_append."""
+    assert kv_new.dtype == torch.bfloat16 and kv_new.dim() == 6 and kv_new.stride(5) == 1
+    st = (ctypes.c_int64 * 5)(*[kv_new.stride(i) for i in range(5)])
+    check("rq_paged_encode_append", _lib.lib().rq_paged_encode_append(
+        ctypes.byref(shape), ctypes.byref(cache.struct), ctypes.byref(paging), _ptr(kv_new), st,
+        _ptr(positions), int(pos_begin), int(kv_new.shape[1]), _stream(stream)))
+
+
+def paged_decode_attention(shape, cache, paging, q, loop_begin, loop_count, pending_kv,
+                           ctx_lens, max_ctx, out, ws, stream=None):
+    check("rq_paged_decode_attention", _lib.lib().rq_paged_decode_attention(
+        ctypes.byref(shape), ctypes.byref(cache.struct), ctypes.byref(paging), _ptr(q),
+        int(loop_begin), int(loop_count), _ptr(pending_kv), _ptr(ctx_lens), int(max_ctx),
+        _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def encode_append(shape, cache, kv_new, positions=None, pos_begin=0, stream=None):

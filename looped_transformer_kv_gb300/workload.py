@@ -134,6 +134,46 @@ class Workload:
         return torch.empty(self.B, self.Hq, loop_count, self.d, dtype=torch.bfloat16,
                            device=self.device)
 
+    # ------------------------------------------------------------------ paged twin
+    def paged_twin(self, spare_pages=0, seed=0, chunk_tokens=2048):
+        """The same tokens in a paged cache (64-token pages scattered at random over a pool of
+        B * capacity / 64 + spare_pages pages).  Returns (cache, paging, block_table)."""
+        B, H, d, L, cap = self.B, self.H, self.d, self.L, self.cap
+        max_pages = cap // rq.PAGE
+        n_pages = B * max_pages + spare_pages
+        rng = np.random.default_rng(seed)
+        table = rng.permutation(n_pages)[: B * max_pages].reshape(B, max_pages).astype(np.int32)
+        bt = torch.from_numpy(table).to(self.device)
+        signs = torch.from_numpy(self.signs_np.transpose(1, 0, 2).copy())
+        pc = rq.PackedCache(self.shape, signs, device=self.device, n_pages=n_pages)
+        paging = rq.make_paging(bt, n_pages)
+        bmax = max(1, min(B, (1 << 28) // max(1, chunk_tokens * 2 * L * H * d)))
+        buf = torch.empty(bmax, chunk_tokens, 2, L, H, d, dtype=torch.bfloat16, device=self.device)
+        st = buf.stride()
+        for b0 in range(0, B, bmax):
+            nb = min(bmax, B - b0)
+            sub = rq.make_shape(nb, self.Hq, H, d, L, cap, self.cfg.res_bits[: L - 1])
+            sub_paging = rq.make_paging(bt[b0:b0 + nb], n_pages)
+            for t0 in range(0, cap, chunk_tokens):
+                nt = min(chunk_tokens, cap - t0)
+                rq.synth_states(self.params, buf, st[:5], b0, nb, t0, nt, 0, L)
+                rq.paged_encode_append(sub, pc, sub_paging, buf[:nb, :nt], pos_begin=t0)
+        del buf
+        return pc, paging, bt
+
+    def decode_paged(self, cache, paging, loop_begin, loop_count, out, ws, pending=True,
+                     stream=None):
+        q = self.q if loop_count == self.L else (
+            self.q_loop[loop_begin] if loop_count == 1 else
+            self.q[:, :, loop_begin:loop_begin + loop_count].contiguous())
+        pend = None
+        if pending:
+            pend = self.pending if loop_count == self.L else (
+                self.pending_loop[loop_begin] if loop_count == 1 else
+                self.pending[:, :, loop_begin:loop_begin + loop_count].contiguous())
+        rq.paged_decode_attention(self.shape, cache, paging, q, loop_begin, loop_count, pend,
+                                  self.ctx_lens, self.max_ctx, out, ws, stream)
+
     # ------------------------------------------------------------------ readback
     def packed_slice(self, b, h, ntok):
         """Host copies of the packed arrays of (sequence b, kv-head h), tokens [0, ntok)."""

@@ -88,3 +88,21 @@ def test_null_pointers_and_ranges_are_rejected(lib):
     assert L.rq_bf16_decode_attention(ctypes.byref(s), None, None, None, 0, 1, None, None, 0,
                                       None, None, 0, None) == 1
     assert L.rq_decode_workspace_bytes(ctypes.byref(s), 0, 10) == 0
+
+
+def test_paging_arguments_are_validated(lib):
+    L = lib.lib()
+    s = _shape(lib, capacity=128)
+    c = lib.RqCache()
+    st = (ctypes.c_int64 * 5)(0, 0, 0, 0, 0)
+    g = lib.RqPaging()
+    g.block_table, g.max_pages, g.n_pages = 16, 2, 8          # non-null dummy table
+    # null paging, missing table, capacity != 64 * max_pages, no pages: rejected before any
+    # pointer is used (the cache arrays are null too, so the paging check must come first or
+    # fail the same way)
+    assert L.rq_paged_decode_attention(ctypes.byref(s), ctypes.byref(c), None, None, 0, 1, None,
+                                       None, 0, None, None, 0, None) == 1
+    assert L.rq_paged_encode_append(ctypes.byref(s), ctypes.byref(c), None, ctypes.c_void_p(16),
+                                    st, None, 0, 1, None) == 1
+    assert L.rq_paged_cache_bytes(ctypes.byref(s), 0) == 0
+    assert L.rq_paged_cache_bytes(ctypes.byref(s), 8) == O.cache_bytes(128, 4, (2, 2, 2), 64, 2, 8)

@@ -1,0 +1,113 @@
+"""Paged cache (block table of 64-token pages) against the contiguous cache, on the GPU.
+
+The same seeded states are encoded into a contiguous cache and into a paged cache whose
+block table scatters every sequence's pages over a larger pool in random order.  Every
+page of the paged arrays must equal the matching 64-token rows of the contiguous arrays
+byte for byte, and the paged decode must return the contiguous decode's outputs bit for bit
+(the contiguous path itself is checked against the fp64 oracle by test_gpu_parity.py).
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import looped_transformer_kv_gb300 as rqm
+    from looped_transformer_kv_gb300.workload import Workload
+
+
+def _cfg(name, **kw):
+    return dataclasses.replace(synth.config_by_name(name), **kw)
+
+
+CASES = [
+    ("pr1_small", {}, [256]),
+    ("layer_1p4b", dict(batch=3, n_q_heads=2, n_kv_heads=2), [257, 64, 1]),
+    ("gqa_deep", dict(batch=2, n_q_heads=8, n_kv_heads=2), [300, 129]),
+    ("mixed_24l", dict(batch=2, n_q_heads=2, n_kv_heads=2), [191, 0]),
+]
+
+
+def _paged_twin(w, spare_pages, seed):
+    """A paged cache holding the same tokens as workload w, pages scattered at random."""
+    pc, paging, bt = w.paged_twin(spare_pages=spare_pages, seed=seed)
+    return pc, paging, bt, bt.cpu().numpy()
+
+
+def _arrays(cache):
+    out = [("ref_codes", kv, cache.ref_codes[kv]) for kv in range(2)]
+    out += [("ref_meta", kv, cache.ref_meta[kv]) for kv in range(2)]
+    for kv in range(2):
+        for l in range(len(cache.res_codes[kv])):
+            out += [("res_codes%d" % l, kv, cache.res_codes[kv][l]),
+                    ("res_meta%d" % l, kv, cache.res_meta[kv][l]),
+                    ("alpha%d" % l, kv, cache.alpha[kv][l])]
+    return out
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_paged_cache_matches_contiguous(case):
+    name, over, ctx = CASES[case]
+    cfg = _cfg(name, **over)
+    cap = -(-(max(ctx) + 2) // 64) * 64
+    w = Workload(cfg, capacity=cap, ctx_lens=ctx, batch=len(ctx))
+    pc, paging, bt, table = _paged_twin(w, spare_pages=5, seed=case)
+    torch.cuda.synchronize()
+    # every page byte for byte
+    for (name_a, kv, contig), (_, _, paged) in zip(_arrays(w.cache), _arrays(pc)):
+        c = contig.view(torch.uint8).reshape(w.B, w.H, cap // 64, 64, -1)
+        p = paged.view(torch.uint8).reshape(pc.n_pages, w.H, 64, -1)
+        for b in range(w.B):
+            got = p[torch.from_numpy(table[b]).long().cuda()]           # [pages][H][64][row]
+            want = c[b].permute(1, 0, 2, 3)                              # [pages][H][64][row]
+            assert torch.equal(got, want), (name_a, kv, b)
+    # decode: all loops at once, each loop alone, a middle range
+    calls = [(0, cfg.n_loops)] + [(l, 1) for l in range(cfg.n_loops)]
+    if cfg.n_loops > 2:
+        calls.append((1, 2))
+    for l0, lc in calls:
+        o1, o2 = w.out_buffer(lc), w.out_buffer(lc)
+        ws1, ws2 = w.workspace(lc), w.workspace(lc)
+        w.decode(l0, lc, o1, ws1)
+        q = w.q[:, :, l0:l0 + lc].contiguous()
+        pend = w.pending[:, :, l0:l0 + lc].contiguous()
+        rqm.rq.paged_decode_attention(w.shape, pc, paging, q, l0, lc, pend, w.ctx_lens,
+                                      w.max_ctx, o2, ws2)
+        torch.cuda.synchronize()
+        assert ws2[:1].view(torch.int32).item() == 0
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)), (l0, lc)
+
+
+def test_paged_table_entry_out_of_range_is_flagged_not_read():
+    cfg = _cfg("pr1_small")
+    w = Workload(cfg, capacity=256, ctx_lens=[200], batch=1)
+    pc, paging, bt, table = _paged_twin(w, spare_pages=0, seed=9)
+    bad = bt.clone()
+    bad[0, 1] = pc.n_pages + 7                    # page 1 of sequence 0: out of range
+    bad_paging = rqm.rq.make_paging(bad, pc.n_pages)
+    L = cfg.n_loops
+    o, ws = w.out_buffer(L), w.workspace(L)
+    rqm.rq.paged_decode_attention(w.shape, pc, bad_paging, w.q, 0, L, w.pending, w.ctx_lens,
+                                  w.max_ctx, o, ws)
+    torch.cuda.synchronize()
+    assert ws[:1].view(torch.int32).item() != 0
+    assert torch.isnan(o.float()).all()
+    # encode: the token whose page is out of range is skipped, the others are written
+    before = [t.clone() for (_, _, t) in _arrays(pc)]
+    kv = torch.zeros(1, 2, 2, L, w.H, w.d, dtype=torch.bfloat16, device="cuda")
+    pos = torch.tensor([[70, 10]], dtype=torch.int32, device="cuda")   # page 1 (bad), page 0
+    rqm.rq.paged_encode_append(w.shape, pc, bad_paging, kv, positions=pos)
+    torch.cuda.synchronize()
+    after = [t for (_, _, t) in _arrays(pc)]
+    changed = [not torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+               for x, y in zip(before, after)]
+    assert any(changed)                            # token 10 (page 0) was written
+    p1 = int(table[0, 1])
+    for x, y in zip(before, after):
+        assert torch.equal(x[p1].view(torch.uint8), y[p1].view(torch.uint8))
