@@ -334,6 +334,22 @@ def gpu_arm(args, cfg):
         t_pg_per = timeit(graph_of(pg_per), iters)
         del pc, paging, bt
         torch.cuda.empty_cache()
+    # serving step: the L per-loop decode calls, the deferred write of the token into slot
+    # ctx_len and the advance of ctx_len, captured once and replayed token after token (the
+    # spare capacity past ctx takes the appended tokens)
+    ctx_srv = w.ctx_lens.clone()
+    ws_srv = w.workspace_for(1, w.cap)
+    t_srv = timeit(graph_of(lambda: w.serving_step(ctx_srv, out1, ws_srv, w.cap)), iters)
+    grown = int((ctx_srv - w.ctx_lens).max().item())
+    # bulk prefill encode: n_pre tokens of every sequence in one call (their own states, so
+    # the cache is rewritten with the same bytes)
+    n_pre = min(2048, ctx)
+    pre = torch.empty(B, n_pre, 2, L, w.H, w.d, dtype=torch.bfloat16, device="cuda")
+    rqm.synth_states(w.params, pre, pre.stride()[:5], 0, B, 0, n_pre, 0, L)
+    t_pre = timeit(graph_of(lambda: rqm.encode_append(w.shape, w.cache, pre, pos_begin=0)), iters)
+    pre_bytes = pre.numel() * 2
+    del pre
+    torch.cuda.empty_cache()
     clk = clocks.stop()
 
     # ---- end to end through the public API with host buffers ----
@@ -399,6 +415,16 @@ def gpu_arm(args, cfg):
         breakdown["speedup_vs_bf16"] = {"multiloop": med(t_bf_multi) / dec_ms,
                                         "perloop": med(t_bf_per) / med(t_per)}
     breakdown["storage_reduction_vs_bf16"] = 1 - (ref_b + sum(res_b)) / (L * 2 * d * 2)
+    m = med(t_srv)
+    breakdown["serving_step"] = {
+        "what": "per-loop decode of all %d loops + encode of the token + ctx advance, one CUDA "
+                "graph replayed %d times (ctx %d..%d)" % (L, len(t_srv), ctx, ctx + grown),
+        "ms": m, "tokens_s": B / (m * 1e-3), "kv_tokens_s": kvtok / (m * 1e-3)}
+    m = med(t_pre)
+    breakdown["prefill_encode"] = {
+        "what": "rq_encode_append of %d tokens x %d sequences in one call" % (n_pre, B),
+        "ms": m, "tokens_s": B * n_pre / (m * 1e-3),
+        "gbs": (pre_bytes + B * n_pre * w.H * (ref_b + sum(res_b))) / (m * 1e-3) / 1e9}
     if t_pg_multi:
         for name, tt, nb, base in (("rq_paged_decode_multiloop", t_pg_multi, bytes_multi, dec_ms),
                                    ("rq_paged_decode_perloop", t_pg_per, bytes_per, med(t_per))):

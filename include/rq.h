@@ -208,6 +208,15 @@ rq_status rq_decode_attention_noalloc(const rq_shape* shape, const rq_cache* cac
                                       int32_t max_ctx, uint16_t* out, void* stream);
 
 /* Human-readable name of a status. */
+/* Serving step support (rit.work summary, "How each pass's KV cache is reconstructed": the
+ * current token's loops are encoded once its final loop ends, then it joins the cache).
+ * Adds n to every ctx_lens[b] on the device, capped at capacity, so that a captured CUDA graph
+ * of one decode step -- the per-loop decode calls, rq_encode_append with positions = ctx_lens
+ * (n_new = 1: the new token goes to slot ctx_len) and this call -- can be replayed token after
+ * token.  ctx_lens: device int32 [batch]; n >= 0. */
+rq_status rq_advance_ctx(int32_t* ctx_lens, int32_t batch, int32_t n, int32_t capacity,
+                         void* stream);
+
 const char* rq_status_str(rq_status status);
 
 #ifdef __cplusplus

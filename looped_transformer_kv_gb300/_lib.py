@@ -16,7 +16,7 @@ EXPORTS = ("rq_cache_bytes", "rq_encode_append", "rq_decode_workspace_bytes",
            "rq_decode_attention", "rq_bf16_decode_attention", "rq_status_str",
            "rq_synth_states", "rq_synth_queries", "rq_decode_noalloc_scratch_bytes",
            "rq_decode_attention_noalloc", "rq_paged_cache_bytes", "rq_paged_encode_append",
-           "rq_paged_decode_attention")
+           "rq_paged_decode_attention", "rq_advance_ctx")
 
 
 class RqShape(ctypes.Structure):
@@ -89,6 +89,8 @@ def lib():
     L.rq_paged_encode_append.restype = i32
     L.rq_paged_decode_attention.argtypes = [S, C, G, _P, i32, i32, _P, _P, i32, _P, _P, sz, _P]
     L.rq_paged_decode_attention.restype = i32
+    L.rq_advance_ctx.argtypes = [_P, i32, i32, i32, _P]
+    L.rq_advance_ctx.restype = i32
     L.rq_status_str.argtypes = [i32]
     L.rq_status_str.restype = ctypes.c_char_p
     P = ctypes.POINTER(RqSynthParams)

@@ -8,6 +8,14 @@
 
 namespace {
 
+__global__ void advance_ctx_kernel(int32_t* ctx_lens, int32_t batch, int32_t n, int32_t cap) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < batch) {
+    const int64_t v = int64_t(ctx_lens[b]) + n;
+    ctx_lens[b] = int32_t(v > cap ? cap : v);
+  }
+}
+
 rq_status check_shape(const rq_shape* s) {
   if (!s) return RQ_ERR_INVALID_ARG;
   if (s->batch <= 0 || s->n_q_heads <= 0 || s->n_kv_heads <= 0 || s->capacity <= 0 ||
@@ -188,6 +196,14 @@ rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k, con
   } catch (...) {
     return RQ_ERR_INTERNAL;
   }
+}
+
+rq_status rq_advance_ctx(int32_t* ctx_lens, int32_t batch, int32_t n, int32_t capacity,
+                         void* stream) {
+  if (!ctx_lens || batch <= 0 || n < 0 || capacity <= 0) return RQ_ERR_INVALID_ARG;
+  advance_ctx_kernel<<<(batch + 127) / 128, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      ctx_lens, batch, n, capacity);
+  return from_cuda(cudaGetLastError());
 }
 
 const char* rq_status_str(rq_status s) {

@@ -93,6 +93,13 @@ def cache_bytes(shape):
     return int(_lib.lib().rq_cache_bytes(ctypes.byref(shape)))
 
 
+def advance_ctx(ctx_lens, n, capacity, stream=None):
+    """rq_advance_ctx: ctx_lens[b] += n on the device (capped at capacity)."""
+    assert ctx_lens.dtype == torch.int32 and ctx_lens.is_contiguous()
+    check("rq_advance_ctx", _lib.lib().rq_advance_ctx(_ptr(ctx_lens), ctx_lens.numel(), int(n),
+                                                      int(capacity), _stream(stream)))
+
+
 def paged_cache_bytes(shape, n_pages):
     return int(_lib.lib().rq_paged_cache_bytes(ctypes.byref(shape), int(n_pages)))
 

@@ -134,6 +134,26 @@ class Workload:
         return torch.empty(self.B, self.Hq, loop_count, self.d, dtype=torch.bfloat16,
                            device=self.device)
 
+    # ------------------------------------------------------------------ serving step
+    def serving_step(self, ctx_lens, out1, ws1, max_ctx, stream=None):
+        """One decode step of the looped model for every sequence, as a server runs it: loop
+        l's query attends over loop l's cache with the current token's loop-l state pending,
+        for l = 0..L-1 in order; then the token's L states are encoded into slot ctx_len
+        (deferred write) and ctx_len advances by one, on the device.  With max_ctx fixed (an
+        upper bound), the sequence of calls can be captured once in a CUDA graph and replayed
+        token after token."""
+        B, L = self.B, self.L
+        for l in range(L):
+            rq.decode_attention(self.shape, self.cache, self.q_loop[l], l, 1, self.pending_loop[l],
+                                ctx_lens, max_ctx, out1[l], ws1, stream)
+        kv_new = self.pending.reshape(B, 1, 2, L, self.H, self.d)
+        rq.encode_append(self.shape, self.cache, kv_new, positions=ctx_lens, stream=stream)
+        rq.advance_ctx(ctx_lens, 1, self.cap, stream)
+
+    def workspace_for(self, loop_count, max_ctx):
+        n = rq.decode_workspace_bytes(self.shape, loop_count, max_ctx)
+        return torch.empty(max(n, 16) // 4 + 4, dtype=torch.float32, device=self.device)
+
     # ------------------------------------------------------------------ paged twin
     def paged_twin(self, spare_pages=0, seed=0, chunk_tokens=2048):
         """The same tokens in a paged cache (64-token pages scattered at random over a pool of
