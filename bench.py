@@ -462,6 +462,75 @@ def gpu_arm(args, cfg):
         dist.destroy_process_group()
 
 
+def budget_arm(args, cfg):
+    """Fixed KV-memory budget per layer: the largest batch whose cache fits, for the packed
+    cache and for the BF16 cache, and decode KV tokens/s of each at its own batch (one JSON
+    line)."""
+    import torch
+
+    import looped_transformer_kv_gb300 as rqm
+    from looped_transformer_kv_gb300.workload import Workload
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    budget = int(args.budget_gb * (1 << 30))
+    cap = max(64, -(-(cfg.ctx + 2) // 64) * 64)
+    L, H, d = cfg.n_loops, cfg.n_kv_heads, cfg.head_dim
+    rq_seq = rqm.rq.cache_bytes(rqm.make_shape(1, cfg.n_q_heads, H, d, L, cap,
+                                               cfg.res_bits[: L - 1]))
+    bf_seq = 2 * H * L * cap * d * 2
+    res = {"experiment": "fixed KV-memory budget per layer", "workload": _workload_desc(cfg),
+           "budget_gib": args.budget_gb, "bytes_per_sequence": {"rq": rq_seq, "bf16": bf_seq}}
+    iters = max(args.steps, 10)
+
+    def timed(fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        for _ in range(max(3, args.warmup)):
+            gr.replay()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(iters):
+            gr.replay()
+        ev[1].record()
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / iters
+
+    for kind in ("rq", "bf16"):
+        B = budget // (rq_seq if kind == "rq" else bf_seq)
+        w = Workload(cfg, capacity=cap, batch=int(B), build_rq=kind == "rq",
+                     build_bf16=kind == "bf16")
+        out, ws = w.out_buffer(L), w.workspace(L)
+        out1, ws1 = [w.out_buffer(1) for _ in range(L)], w.workspace(1)
+        dec = w.decode if kind == "rq" else w.decode_bf16
+        t_multi = timed(lambda: dec(0, L, out, ws))
+
+        def per():
+            for l in range(L):
+                dec(l, 1, out1[l], ws1)
+
+        t_per = timed(per)
+        kvtok = B * cfg.ctx * L
+        res[kind] = {"batch": int(B), "cache_gib": B * (rq_seq if kind == "rq" else bf_seq) / 2**30,
+                     "multiloop_ms": t_multi, "multiloop_kv_tokens_s": kvtok / (t_multi * 1e-3),
+                     "perloop_ms": t_per, "perloop_kv_tokens_s": kvtok / (t_per * 1e-3)}
+        del w, out, ws, out1, ws1
+        torch.cuda.empty_cache()
+    res["batch_ratio"] = res["rq"]["batch"] / res["bf16"]["batch"]
+    res["throughput_ratio_multiloop"] = (res["rq"]["multiloop_kv_tokens_s"] /
+                                         res["bf16"]["multiloop_kv_tokens_s"])
+    res["throughput_ratio_perloop"] = (res["rq"]["perloop_kv_tokens_s"] /
+                                       res["bf16"]["perloop_kv_tokens_s"])
+    print(json.dumps(res), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,6 +541,8 @@ def main():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-paged", action="store_true")
+    ap.add_argument("--budget-gb", type=float, default=0.0,
+                    help="run the fixed KV-memory budget experiment (GiB per layer) instead")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -482,7 +553,10 @@ def main():
     else:
         from __graft_entry__ import build
         build()
-        gpu_arm(args, cfg)
+        if args.budget_gb > 0:
+            budget_arm(args, cfg)
+        else:
+            gpu_arm(args, cfg)
 
 
 if __name__ == "__main__":
