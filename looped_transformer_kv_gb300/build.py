@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "librq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["rq_api.cu", "rq_encode.cu", "rq_decode.cu", "rq_decode_mma.cu", "rq_bf16.cu",
+SOURCES = ["rq_api.cu", "rq_encode.cu", "rq_decode.cu", "rq_decode_mma.cu", "rq_decode_mma_paged.cu", "rq_bf16.cu",
            "rq_synth.cu", "rq_noalloc.cu"]
 
 
