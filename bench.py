@@ -31,11 +31,12 @@ METRIC = "decode-attn KV tokens/s at 1 GB300, HBM GB/s vs peak, vs in-build BF16
 # of the split kernel, from one ncu capture (profiles/), keyed by the kernel sources they
 # were taken on; any change to those sources makes the figure stale (reported as null).
 KERNEL_SOURCES = ("looped_transformer_kv_gb300/csrc/rq_decode_mma.cu",
+                  "looped_transformer_kv_gb300/csrc/rq_decode_mma.cuh",
                   "looped_transformer_kv_gb300/csrc/rq_ptx.cuh",
                   "looped_transformer_kv_gb300/csrc/rq_common.cuh",
                   "looped_transformer_kv_gb300/csrc/rq_kernels.h")
 TRAFFIC = {
-    ("a20cf97e42d31401", "layer_1p4b"): 484052736 + 13730048,  # profiles/rq_mma_kernel_layer_1p4b.md
+    ("21adc72a070bffe7", "layer_1p4b"): 484533248 + 11348992,  # profiles/rq_mma_kernel_layer_1p4b.md
 }
 
 
