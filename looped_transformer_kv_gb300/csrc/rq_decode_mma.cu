@@ -35,11 +35,14 @@ cudaError_t prepare_kernels() {
   return err[dev];
 }
 
+// Blocks of at most 4 query columns run the packed variant (low parts in MMA columns 4-7).
+bool packed_block(const QueryBlock& bq) { return bq.gw * bq.nl <= 4; }
+
 // CTAs of a kernel variant resident per SM with `smem` bytes of dynamic shared memory.
-int resident_ctas(int D, bool res4, int nr, size_t smem) {
+int resident_ctas(int D, bool res4, int nr, bool packed, size_t smem) {
   int n = 0;
   if (prepare_kernels() == cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, res4, nr, false, false), kW * 32, smem) ==
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, res4, nr, false, packed), kW * 32, smem) ==
           cudaSuccess &&
       n > 0)
     return n;
@@ -96,7 +99,7 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
   for (int stages = 3; stages >= 2; --stages) {
     const size_t sm = smem_layout(D, res4, stages, a.stage_bytes, n_pg).total;
     if (sm > 200 * 1024) continue;
-    const int ctas = resident_ctas(D, res4, bq.nr, sm);
+    const int ctas = resident_ctas(D, res4, bq.nr, packed_block(bq), sm);
     if (ctas > best_ctas) {
       best_ctas = ctas;
       a.n_stages = stages;
@@ -154,7 +157,7 @@ SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int 
   for (int i = 0; i < nb; ++i) {
     BlockLaunch bl;
     if (!build_block(s, dummy, blocks[i], 0, bl)) continue;
-    const int n = resident_ctas(s.head_dim, bl.res4, blocks[i].nr, bl.smem);
+    const int n = resident_ctas(s.head_dim, bl.res4, blocks[i].nr, packed_block(blocks[i]), bl.smem);
     if (ctas == 0 || n < ctas) ctas = n;
   }
   return plan_splits_for(s, max_ctx, ctas > 0 ? ctas : 1, kT);
@@ -196,8 +199,7 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.tokens_per_split = tokens_per_split;
     a.scale_log2 = scale * kLog2e;
     dim3 grid(n_splits, s.n_kv_heads, s.batch);
-    const bool packed = blocks[bi].gw * blocks[bi].nl <= 4;
-    pick(s.head_dim, bl.res4, blocks[bi].nr, paging != nullptr, packed)<<<grid, kW * 32, bl.smem, stream>>>(a);
+    pick(s.head_dim, bl.res4, blocks[bi].nr, paging != nullptr, packed_block(blocks[bi]))<<<grid, kW * 32, bl.smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

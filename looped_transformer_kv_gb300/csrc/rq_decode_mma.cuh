@@ -203,8 +203,10 @@ __device__ __forceinline__ void weights_to_b_packed(float w00, float w01, float 
 // PAGED: tiles are found through the block table of a paged cache.
 // HL: at most 4 query columns; the low parts of the query and weight splits ride in MMA
 // columns 4-7 (one MMA where two would be), columns 4-7 being no query's.
+// Blocks of the final loop alone (NRT 0) are held to 128 registers for four resident CTAs per
+// SM; the others take up to 168 for three.
 template <int D, bool RES4, int NRT, bool PAGED, bool HL>
-__global__ void __launch_bounds__(kW * 32, 3) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
+__global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NG = D / 32;
   constexpr int NQ = kNQ;
   constexpr int P = D / 32;          // channels per lane in the query prep
