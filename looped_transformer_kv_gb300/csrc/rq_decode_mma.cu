@@ -9,9 +9,10 @@ namespace rq {
 namespace {
 
 
-KernelFn pick(int D, bool res4, int nr, bool paged, bool packed) {
-  if (paged) return pick_paged(D, res4, nr, packed);
-  return packed ? pick_pg<false, true>(D, res4, nr) : pick_pg<false, false>(D, res4, nr);
+KernelFn pick(int D, bool res4, int nr, bool paged, int pk) {
+  if (paged) return pick_paged(D, res4, nr, pk);
+  if (pk == 2) return pick_pg<false, 2>(D, res4, nr);
+  return pk == 1 ? pick_pg<false, 1>(D, res4, nr) : pick_pg<false, 0>(D, res4, nr);
 }
 
 // Opt every kernel variant in to the largest dynamic shared memory, once per device.
@@ -24,9 +25,9 @@ cudaError_t prepare_kernels() {
     err[dev] = cudaSuccess;
     for (int D : {64, 128})
       for (bool r4 : {false, true})
-        for (int pk = 0; pk < 4; ++pk)   // contiguous / paged, each packed or not
+        for (int v = 0; v < 6; ++v)   // contiguous / paged, each with the three packings
           for (int nr = -1; nr <= kMaxResPerBlock; ++nr) {
-            cudaError_t e = cudaFuncSetAttribute(pick(D, r4, nr, pk >= 2, pk & 1),
+            cudaError_t e = cudaFuncSetAttribute(pick(D, r4, nr, v >= 3, v % 3),
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  200 * 1024);
             if (e != cudaSuccess) err[dev] = e;
@@ -35,14 +36,18 @@ cudaError_t prepare_kernels() {
   return err[dev];
 }
 
-// Blocks of at most 4 query columns run the packed variant (low parts in MMA columns 4-7).
-bool packed_block(const QueryBlock& bq) { return bq.gw * bq.nl <= 4; }
+// Packing of the MMA columns for a block: one query column -> its channel groups take the
+// columns (2); at most 4 -> low parts in columns 4-7 (1); else high and low parts in two MMAs.
+int block_packing(const QueryBlock& bq) {
+  const int cols = bq.gw * bq.nl;
+  return cols == 1 ? 2 : (cols <= 4 ? 1 : 0);
+}
 
 // CTAs of a kernel variant resident per SM with `smem` bytes of dynamic shared memory.
-int resident_ctas(int D, bool res4, int nr, bool packed, size_t smem) {
+int resident_ctas(int D, bool res4, int nr, int pk, size_t smem) {
   int n = 0;
   if (prepare_kernels() == cudaSuccess &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, res4, nr, false, packed), kW * 32, smem) ==
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pick(D, res4, nr, false, pk), kW * 32, smem) ==
           cudaSuccess &&
       n > 0)
     return n;
@@ -99,7 +104,7 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
   for (int stages = 3; stages >= 2; --stages) {
     const size_t sm = smem_layout(D, res4, stages, a.stage_bytes, n_pg).total;
     if (sm > 200 * 1024) continue;
-    const int ctas = resident_ctas(D, res4, bq.nr, packed_block(bq), sm);
+    const int ctas = resident_ctas(D, res4, bq.nr, block_packing(bq), sm);
     if (ctas > best_ctas) {
       best_ctas = ctas;
       a.n_stages = stages;
@@ -157,7 +162,7 @@ SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int 
   for (int i = 0; i < nb; ++i) {
     BlockLaunch bl;
     if (!build_block(s, dummy, blocks[i], 0, bl)) continue;
-    const int n = resident_ctas(s.head_dim, bl.res4, blocks[i].nr, packed_block(blocks[i]), bl.smem);
+    const int n = resident_ctas(s.head_dim, bl.res4, blocks[i].nr, block_packing(blocks[i]), bl.smem);
     if (ctas == 0 || n < ctas) ctas = n;
   }
   return plan_splits_for(s, max_ctx, ctas > 0 ? ctas : 1, kT);
@@ -199,7 +204,7 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.tokens_per_split = tokens_per_split;
     a.scale_log2 = scale * kLog2e;
     dim3 grid(n_splits, s.n_kv_heads, s.batch);
-    pick(s.head_dim, bl.res4, blocks[bi].nr, paging != nullptr, packed_block(blocks[bi]))<<<grid, kW * 32, bl.smem, stream>>>(a);
+    pick(s.head_dim, bl.res4, blocks[bi].nr, paging != nullptr, block_packing(blocks[bi]))<<<grid, kW * 32, bl.smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

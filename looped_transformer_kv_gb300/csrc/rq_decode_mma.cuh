@@ -201,12 +201,15 @@ __device__ __forceinline__ void weights_to_b_packed(float w00, float w01, float 
 
 // NRT >= 0: the block's number of residual loops, fixed at compile time; -1: read at run time.
 // PAGED: tiles are found through the block table of a paged cache.
-// HL: at most 4 query columns; the low parts of the query and weight splits ride in MMA
-// columns 4-7 (one MMA where two would be), columns 4-7 being no query's.
-// Blocks of the final loop alone (NRT 0) are held to 128 registers for four resident CTAs per
-// SM; the others take up to 168 for three.
-template <int D, bool RES4, int NRT, bool PAGED, bool HL>
-__global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
+// PK (packing of the MMA's 8 columns): 0 = up to 8 query columns, high and low parts of the
+// splits in two MMAs; 1 = at most 4 query columns, the low parts of the query and weight splits
+// ride in columns 4-7 (one MMA where two would be); 2 = one query column, whose channel groups
+// take the columns: group g's high parts in column g, its low parts in column g + 4, so that
+// every lane of a fragment row scales distinct groups and one transpose serves every group.
+// Blocks of the final loop alone (NRT 0) and single-column blocks with a 2-bit residual loop
+// are held to 128 registers for four resident CTAs per SM; the others take up to 168 for three.
+template <int D, bool RES4, int NRT, bool PAGED, int PK>
+__global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 : 3) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NG = D / 32;
   constexpr int NQ = kNQ;
   constexpr int P = D / 32;          // channels per lane in the query prep
@@ -214,6 +217,9 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
   constexpr int RB2 = D / 4;         // bytes of a 2-bit row
   constexpr int MT = D / 16;         // 16-channel m-tiles of the value phase (2 per group)
   constexpr bool PER_LOOP = NRT >= 1 && NRT <= 3;   // one residual score accumulator per loop
+  constexpr bool HL = PK >= 1;                      // low parts in columns 4-7
+  constexpr bool SC = PK == 2;                      // one query column, groups in columns
+  static_assert(!SC || (NRT == 0 || NRT == 1) && D == 128, "single-column blocks: D 128, one loop");
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -409,11 +415,13 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
 #pragma unroll
     for (int j = 0; j < P; ++j) {
       if (HL && n >= 4) break;
+      if (SC && n != 0) break;       // (SC: columns 1-7 are the groups' slots)
       const int ch = lane * P + j, gq = ch >> 5, cl = ch & 31;
+      const int ns = SC ? gq : n;    // fragment column of the high part
       const float vq = v[j] * qscale, rq = rr[j] * qscale;
       {  // 4-bit mapping: slot (c4, s, hi, e) <- channel 8 c4 + 2 s + hi + 4 e, scale 16^-hi
         const int c4 = cl >> 3, w8 = cl & 7, s = (w8 >> 1) & 1, hi = w8 & 1, e = w8 >> 2;
-        const int idx = (gq * 2 + s) * 32 + n * 4 + c4;
+        const int idx = (gq * 2 + s) * 32 + ns * 4 + c4;
         __half* dq = reinterpret_cast<__half*>(&QF[idx]);
         __half* dql = HL ? reinterpret_cast<__half*>(&QF[idx + 16]) : dq + 4;
         split_half(hi ? vq * 0.0625f : vq, dq[hi * 2 + e], dql[hi * 2 + e]);
@@ -427,7 +435,7 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
         const int e = (cl >> 3) & 1, cq = 2 * (cl >> 4) + ((cl & 7) >> 2), jj = cl & 3;
         const int s = jj >> 1, hi = jj & 1;
         const float sc = (jj == 0) ? 1.f : (jj == 1) ? 0.25f : (jj == 2) ? 0.0625f : 0.015625f;
-        const int idx = (gq * 2 + s) * 32 + n * 4 + cq;
+        const int idx = (gq * 2 + s) * 32 + ns * 4 + cq;
         __half* dr = reinterpret_cast<__half*>(&QR2[idx]);
         __half* drl = HL ? reinterpret_cast<__half*>(&QR2[idx + 16]) : dr + 4;
         split_half(rq * sc, dr[hi * 2 + e], drl[hi * 2 + e]);
@@ -442,7 +450,9 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     riD[e] = col_ri(HL ? (2 * c + e) & 3 : 2 * c + e);   // HL: the column whose low parts these are
-    const int rc = riD[e] < 0 ? 0 : riD[e];
+    // (one residual loop: both columns' metadata is the same loop's, at a constant address,
+    // so it is loaded and converted once)
+    const int rc = (NRT == 1 || riD[e] < 0) ? 0 : riD[e];
     krmD[e] = FIXED ? F_RES + rc * F_RS + F_KRM : pick_int(a.off_krm, rc);
     kaD[e] = FIXED ? F_RES + rc * F_RS + F_KA : pick_int(a.off_ka, rc);
     vaD[e] = FIXED ? F_RES + rc * F_RS + F_VA : pick_int(a.off_va, rc);
@@ -450,6 +460,18 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
   }
   const int riB = col_ri(HL ? r & 3 : r);
   const bool low_lane = HL && c >= 2;   // fragment columns 4-7: low parts
+  // SC: fragment columns 2c + e hold group gp + e (lanes c >= 2 its low parts); the offset
+  // terms of the scores take the group sums in the high lanes only
+  const int gp = 2 * (c & 1);
+  float qsS[2] = {0.f, 0.f}, qrsS[2] = {0.f, 0.f};
+  if constexpr (SC) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      if (!low_lane) {
+        qsS[e] = Qsum[(gp + e) * NQ];
+        if (NRT == 1) qrsS[e] = QRsum[(gp + e) * NQ];
+      }
+  }
   // loop_mask[e][ri]: all ones where column 2c + e belongs to residual loop ri
   uint32_t loop_mask[2][PER_LOOP ? NRT : 1];
 #pragma unroll
@@ -489,7 +511,84 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
 
       // ---------------------------------------------------------------- scores
       float sc[4];
-      {
+      if constexpr (SC) {
+        // one accumulator for every group: column n holds group n & 3 (n >= 4: low parts)
+        float D0[4] = {0.f, 0.f, 0.f, 0.f}, Dr[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t kw0[NG], kw1[NG];
+        load_words<NG>(sb + o_kc + tr0 * RB4 + c * NG * 4, kw0);
+        load_words<NG>(sb + o_kc + tr1 * RB4 + c * NG * 4, kw1);
+#pragma unroll
+        for (int gq = 0; gq < NG; ++gq)
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            uint32_t a0, a2, a1, a3;
+            a_pairs_4bit(kw0[gq], s, a0, a2);
+            a_pairs_4bit(kw1[gq], s, a1, a3);
+            const uint2 bq = *reinterpret_cast<const uint2*>(&QF[(gq * 2 + s) * 32 + lane]);
+            mma_f16(D0, a0, a1, a2, a3, bq.x, bq.y);
+          }
+        if (NRT == 1) {   // the block's residual loop
+          const bool two = !RES4 || a.rbits[0] == 2;
+#pragma unroll
+          for (int gq = 0; gq < NG; ++gq) {
+            uint32_t wl, wh;
+            if (two) {
+              const int off = o_krc(0) + ((c >> 1) * NG + gq) * 4;
+              wl = lds32(sb + off + tr0 * RB2) >> (8 * (c & 1));
+              wh = lds32(sb + off + tr1 * RB2) >> (8 * (c & 1));
+            } else {
+              const int off = o_krc(0) + (c * NG + gq) * 4;
+              wl = lds32(sb + off + tr0 * RB4);
+              wh = lds32(sb + off + tr1 * RB4);
+            }
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              uint32_t a0, a1, a2, a3;
+              if (two) {
+                a_pairs_2bit(wl, s, a0, a2);
+                a_pairs_2bit(wh, s, a1, a3);
+              } else {
+                a_pairs_4bit(wl, s, a0, a2);
+                a_pairs_4bit(wh, s, a1, a3);
+              }
+              const int fi = (gq * 2 + s) * 32 + lane;
+              const uint2 bq = *reinterpret_cast<const uint2*>((RES4 && !two) ? &QR4[fi] : &QR2[fi]);
+              mma_f16(Dr, a0, a1, a2, a3, bq.x, bq.y);
+            }
+          }
+        }
+        // step and offset of this lane's two groups for tokens tr0 and tr1
+        const uint2 m0 = *reinterpret_cast<const uint2*>(sb + o_km + (tr0 * NG + gp) * 4);
+        const uint2 m1 = *reinterpret_cast<const uint2*>(sb + o_km + (tr1 * NG + gp) * 4);
+        float x[4];
+        {
+          const float2 s00 = meta_f2(m0.x), s01 = meta_f2(m0.y);
+          const float2 s10 = meta_f2(m1.x), s11 = meta_f2(m1.y);
+          x[0] = fmaf(s00.x, D0[0], s00.y * qsS[0]);
+          x[1] = fmaf(s01.x, D0[1], s01.y * qsS[1]);
+          x[2] = fmaf(s10.x, D0[2], s10.y * qsS[0]);
+          x[3] = fmaf(s11.x, D0[3], s11.y * qsS[1]);
+        }
+        if (NRT == 1) {   // a_t * reference part + residual part
+          const uint2 r0 = *reinterpret_cast<const uint2*>(sb + krmD[0] + (tr0 * NG + gp) * 4);
+          const uint2 r1 = *reinterpret_cast<const uint2*>(sb + krmD[0] + (tr1 * NG + gp) * 4);
+          const float al0 = ld_half(sb + kaD[0] + tr0 * 2), al1 = ld_half(sb + kaD[0] + tr1 * 2);
+          const float2 t00 = meta_f2(r0.x), t01 = meta_f2(r0.y);
+          const float2 t10 = meta_f2(r1.x), t11 = meta_f2(r1.y);
+          x[0] = fmaf(al0, x[0], fmaf(t00.x, Dr[0], t00.y * qrsS[0]));
+          x[1] = fmaf(al0, x[1], fmaf(t01.x, Dr[1], t01.y * qrsS[1]));
+          x[2] = fmaf(al1, x[2], fmaf(t10.x, Dr[2], t10.y * qrsS[0]));
+          x[3] = fmaf(al1, x[3], fmaf(t11.x, Dr[3], t11.y * qrsS[1]));
+        }
+        // the token's score: its groups and parts over the 4 lanes of the row
+        float s_0 = x[0] + x[1], s_1 = x[2] + x[3];
+        s_0 += __shfl_xor_sync(RQ_FULL_MASK, s_0, 1);
+        s_1 += __shfl_xor_sync(RQ_FULL_MASK, s_1, 1);
+        s_0 += __shfl_xor_sync(RQ_FULL_MASK, s_0, 2);
+        s_1 += __shfl_xor_sync(RQ_FULL_MASK, s_1, 2);
+        sc[0] = sc[1] = v0 ? s_0 * code_unit : -INFINITY;
+        sc[2] = sc[3] = v1 ? s_1 * code_unit : -INFINITY;
+      } else {
         float R[4], E[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) R[k] = E[k] = 0.f;
@@ -665,7 +764,7 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
               if (RES4) accE4[m][k] *= corr[k & 1];
             }
 #pragma unroll
-          for (int g = 0; g < NG; ++g)
+          for (int g = 0; g < (SC ? 1 : NG); ++g)   // (SC: entry 0 holds the lane's two groups)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               offR[g][e] *= corr[e];
@@ -679,7 +778,98 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
       }
 
       // ---------------------------------------------------------------- values
-      {
+      if constexpr (SC) {
+        // weights of tokens tr0, tr1 (the row's lanes all hold its p): p * a for the reference,
+        // p for the residual; this lane scales them by the steps of its two groups, and one
+        // transpose per token half moves them to the B operand, where column n holds group
+        // n & 3 (n >= 4: low parts); each group's MMAs keep their own columns
+        float pa0 = p[0], pa1 = p[2], pe0 = 0.f, pe1 = 0.f;
+        if (NRT == 1) {
+          pe0 = p[0];
+          pe1 = p[2];
+          pa0 *= ld_half(sb + vaD[0] + tr0 * 2);
+          pa1 *= ld_half(sb + vaD[0] + tr1 * 2);
+        }
+        uint2 n0 = *reinterpret_cast<const uint2*>(sb + o_vm + (tr0 * NG + gp) * 4);
+        uint2 n1 = *reinterpret_cast<const uint2*>(sb + o_vm + (tr1 * NG + gp) * 4);
+        if (partial) {   // rows past the context: zero weights and steps whatever the slots hold
+          pa0 = v0 ? pa0 : 0.f;
+          pa1 = v1 ? pa1 : 0.f;
+          pe0 = v0 ? pe0 : 0.f;
+          pe1 = v1 ? pe1 : 0.f;
+          n0 = v0 ? n0 : make_uint2(0u, 0u);
+          n1 = v1 ? n1 : make_uint2(0u, 0u);
+        }
+        {
+          const float2 u00 = meta_f2(n0.x), u01 = meta_f2(n0.y);
+          const float2 u10 = meta_f2(n1.x), u11 = meta_f2(n1.y);
+          offR[0][0] = fmaf(pa0, u00.y, fmaf(pa1, u10.y, offR[0][0]));
+          offR[0][1] = fmaf(pa0, u01.y, fmaf(pa1, u11.y, offR[0][1]));
+          uint32_t b0, b1;
+          weights_to_b_packed(pa0 * u00.x, pa0 * u01.x, pa1 * u10.x, pa1 * u11.x, low_lane, b0, b1);
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const bool mine = (r & 3) == g;   // this lane's B column is one of group g's
+            const uint32_t g0 = mine ? b0 : 0u, g1 = mine ? b1 : 0u;
+            const uint32_t W0 = lds32(sb + o_vc + p0 * D + ((8 * g + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
+            const uint32_t W1 = lds32(sb + o_vc + p1 * D + ((8 * g + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
+#pragma unroll
+            for (int mtg = 0; mtg < 2; ++mtg) {
+              uint32_t x0, x1, x2, x3;
+              a_pairs_4bit<true>(W0, mtg, x0, x1);
+              a_pairs_4bit<true>(W1, mtg, x2, x3);
+              mma_f16(accR[2 * g + mtg], x0, x1, x2, x3, g0, g1);
+            }
+          }
+        }
+        if (NRT == 1) {
+          uint2 q0 = *reinterpret_cast<const uint2*>(sb + vrmD[0] + (tr0 * NG + gp) * 4);
+          uint2 q1 = *reinterpret_cast<const uint2*>(sb + vrmD[0] + (tr1 * NG + gp) * 4);
+          if (partial) {
+            q0 = v0 ? q0 : make_uint2(0u, 0u);
+            q1 = v1 ? q1 : make_uint2(0u, 0u);
+          }
+          const float2 u00 = meta_f2(q0.x), u01 = meta_f2(q0.y);
+          const float2 u10 = meta_f2(q1.x), u11 = meta_f2(q1.y);
+          offE[0][0] = fmaf(pe0, u00.y, fmaf(pe1, u10.y, offE[0][0]));
+          offE[0][1] = fmaf(pe0, u01.y, fmaf(pe1, u11.y, offE[0][1]));
+          uint32_t b0, b1;
+          weights_to_b_packed(pe0 * u00.x, pe0 * u01.x, pe1 * u10.x, pe1 * u11.x, low_lane, b0, b1);
+          const bool two = !RES4 || a.rbits[0] == 2;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const bool mine = (r & 3) == g;
+            const uint32_t g0 = mine ? b0 : 0u, g1 = mine ? b1 : 0u;
+            if (two) {
+              const int sh = 8 * (r & 1);
+              const int u = 4 * g + (r >> 1);
+              const uint32_t W0 =
+                  lds32(sb + o_vrc(0) + p0 * (2 * RB2) + (u ^ v_unit_swizzle(p0, D / 8)) * 4) >> sh;
+              const uint32_t W1 =
+                  lds32(sb + o_vrc(0) + p1 * (2 * RB2) + (u ^ v_unit_swizzle(p1, D / 8)) * 4) >> sh;
+#pragma unroll
+              for (int mtg = 0; mtg < 2; ++mtg) {
+                uint32_t x0, x1, x2, x3;
+                a_pairs_2bit<true>(W0, mtg, x0, x1);
+                a_pairs_2bit<true>(W1, mtg, x2, x3);
+                mma_f16(accE2[2 * g + mtg], x0, x1, x2, x3, g0, g1);
+              }
+            } else if (RES4) {
+              const uint32_t W0 =
+                  lds32(sb + o_vrc(0) + p0 * D + ((8 * g + r) ^ v_unit_swizzle(p0, D / 4)) * 4);
+              const uint32_t W1 =
+                  lds32(sb + o_vrc(0) + p1 * D + ((8 * g + r) ^ v_unit_swizzle(p1, D / 4)) * 4);
+#pragma unroll
+              for (int mtg = 0; mtg < 2; ++mtg) {
+                uint32_t x0, x1, x2, x3;
+                a_pairs_4bit<true>(W0, mtg, x0, x1);
+                a_pairs_4bit<true>(W1, mtg, x2, x3);
+                mma_f16(accE4[RES4 ? 2 * g + mtg : 0], x0, x1, x2, x3, g0, g1);
+              }
+            }
+          }
+        }
+      } else {
         // p * a (reference weights before the step) and p (residual weights before the step)
         // of this lane's score elements; slots past the context may hold any bits
         float pa[4], pe[4];
@@ -844,7 +1034,7 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
     v += __shfl_xor_sync(RQ_FULL_MASK, v, 16);
     lsum[e] = v;
 #pragma unroll
-    for (int g = 0; g < NG; ++g) {
+    for (int g = 0; g < (SC ? 1 : NG); ++g) {
       float x = offR[g][e], y = offE[g][e];
       x += __shfl_xor_sync(RQ_FULL_MASK, x, 4);
       y += __shfl_xor_sync(RQ_FULL_MASK, y, 4);
@@ -888,8 +1078,31 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
   // columns of the block only)
   constexpr int BS = 2 * D + 4;
   float* buf = reinterpret_cast<float*>(smem);
+  if constexpr (SC) {
+    // the block's one column: group g (channels 32 g ..) sits in lane column c = g / 2,
+    // element e = g % 2, high and low parts added above
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
+    for (int g = 0; g < NG; ++g) {
+      if ((g >> 1) != c) continue;
+      const int e = g & 1;
+      float* o = buf + (warp * NQ) * BS;
+      float vr[4], ve[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int mtg = j >> 1, hh = j & 1, k = 2 * hh + e;
+        const float sc4 = hh ? 0.0625f : 1.f;
+        const float sc2 = 1.f / float(1 << (2 * j));
+        vr[j] = fmaf(accR[2 * g + mtg][k], sc4, offR[0][e]) * f[e];
+        float x = fmaf(accE2[2 * g + mtg][k], sc2, offE[0][e]);
+        if (RES4) x = fmaf(accE4[RES4 ? 2 * g + mtg : 0][k], sc4, x);
+        ve[j] = x * f[e];
+      }
+      *reinterpret_cast<float4*>(o + 32 * g + 4 * r) = make_float4(vr[0], vr[1], vr[2], vr[3]);
+      *reinterpret_cast<float4*>(o + D + 32 * g + 4 * r) = make_float4(ve[0], ve[1], ve[2], ve[3]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 2 && !SC; ++e) {
     const int n = 2 * c + e;
     if (!(n / blk.gw < blk.nl && blk.gi0 + n % blk.gw < a.g)) continue;
     float* o = buf + (warp * NQ + n) * BS;
@@ -950,38 +1163,46 @@ __global__ void __launch_bounds__(kW * 32, NRT == 0 ? 4 : 3) rq_mma_kernel(const
   }
 }
 
-template <int D, bool PG, bool HL>
+template <int D, bool PG, int PK>
 KernelFn pick_generic(bool res4) {
-  return res4 ? rq_mma_kernel<D, true, -1, PG, HL> : rq_mma_kernel<D, false, -1, PG, HL>;
+  return res4 ? rq_mma_kernel<D, true, -1, PG, PK> : rq_mma_kernel<D, false, -1, PG, PK>;
 }
 
 // Variants with the residual-loop count fixed at compile time, for the common blocks: one
 // loop of a per-loop call (0 or 1 residual), two loops of a 4-query-head GQA block (2) and
-// all four loops of a 4-loop model (3); each for a contiguous and for a paged cache, and
-// (contiguous) with the low parts packed into free MMA columns for blocks of <= 4 columns.
-template <bool PG, bool HL>
+// all four loops of a 4-loop model (3); each for a contiguous and for a paged cache and for
+// each packing of the MMA columns.  Single-column packing exists for head dim 128 and one
+// loop; other blocks given it take the 4-column packing.
+template <bool PG, int PK>
 KernelFn pick_pg(int D, bool res4, int nr) {
-  if (D == 128 && !res4) {
-    if (nr == 0) return rq_mma_kernel<128, false, 0, PG, HL>;
-    if (nr == 1) return rq_mma_kernel<128, false, 1, PG, HL>;
-    if (nr == 2) return rq_mma_kernel<128, false, 2, PG, HL>;
-    if (nr == 3) return rq_mma_kernel<128, false, 3, PG, HL>;
+  if constexpr (PK == 2) {
+    if (D == 128 && !res4 && nr == 0) return rq_mma_kernel<128, false, 0, PG, 2>;
+    if (D == 128 && !res4 && nr == 1) return rq_mma_kernel<128, false, 1, PG, 2>;
+    if (D == 128 && res4 && nr == 1) return rq_mma_kernel<128, true, 1, PG, 2>;
+    return pick_pg<PG, 1>(D, res4, nr);
+  } else {
+    if (D == 128 && !res4) {
+      if (nr == 0) return rq_mma_kernel<128, false, 0, PG, PK>;
+      if (nr == 1) return rq_mma_kernel<128, false, 1, PG, PK>;
+      if (nr == 2) return rq_mma_kernel<128, false, 2, PG, PK>;
+      if (nr == 3) return rq_mma_kernel<128, false, 3, PG, PK>;
+    }
+    if (D == 128 && res4) {
+      if (nr == 1) return rq_mma_kernel<128, true, 1, PG, PK>;
+      if (nr == 3) return rq_mma_kernel<128, true, 3, PG, PK>;
+    }
+    if (D == 64 && !res4) {
+      if (nr == 0) return rq_mma_kernel<64, false, 0, PG, PK>;
+      if (nr == 1) return rq_mma_kernel<64, false, 1, PG, PK>;
+      if (nr == 3) return rq_mma_kernel<64, false, 3, PG, PK>;
+    }
+    return D == 128 ? pick_generic<128, PG, PK>(res4) : pick_generic<64, PG, PK>(res4);
   }
-  if (D == 128 && res4) {
-    if (nr == 1) return rq_mma_kernel<128, true, 1, PG, HL>;
-    if (nr == 3) return rq_mma_kernel<128, true, 3, PG, HL>;
-  }
-  if (D == 64 && !res4) {
-    if (nr == 0) return rq_mma_kernel<64, false, 0, PG, HL>;
-    if (nr == 1) return rq_mma_kernel<64, false, 1, PG, HL>;
-    if (nr == 3) return rq_mma_kernel<64, false, 3, PG, HL>;
-  }
-  return D == 128 ? pick_generic<128, PG, HL>(res4) : pick_generic<64, PG, HL>(res4);
 }
 
 }  // namespace
 
 // kernel of the paged-cache variants (rq_decode_mma_paged.cu)
-KernelFn pick_paged(int D, bool res4, int nr, bool packed);
+KernelFn pick_paged(int D, bool res4, int nr, int pk);
 
 }  // namespace rq

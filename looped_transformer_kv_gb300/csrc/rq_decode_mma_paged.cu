@@ -4,8 +4,9 @@
 
 namespace rq {
 
-KernelFn pick_paged(int D, bool res4, int nr, bool packed) {
-  return packed ? pick_pg<true, true>(D, res4, nr) : pick_pg<true, false>(D, res4, nr);
+KernelFn pick_paged(int D, bool res4, int nr, int pk) {
+  if (pk == 2) return pick_pg<true, 2>(D, res4, nr);
+  return pk == 1 ? pick_pg<true, 1>(D, res4, nr) : pick_pg<true, 0>(D, res4, nr);
 }
 
 }  // namespace rq
