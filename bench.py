@@ -254,7 +254,10 @@ def gpu_arm(args, cfg):
                               positions=pos_new)
 
     g = w.Hq // w.H
-    launches_per_step = NL * (math.ceil(g * L / 8) + 1 + 1)
+    # split-kernel blocks, the combine (single-column calls combine inside the split kernel),
+    # the encode
+    combine = 0 if (g * L == 1 and w.d == 128) else 1
+    launches_per_step = NL * (math.ceil(g * L / 8) + combine + 1)
 
     def graph_of(fn):
         """Capture fn (a sequence of library calls on the current stream) in a CUDA graph."""

@@ -153,7 +153,7 @@ rq_status rq_paged_encode_append(const rq_shape* shape, const rq_cache* cache,
 size_t rq_decode_workspace_bytes(const rq_shape* s, int32_t loop_count, int32_t max_ctx) {
   if (check_shape(s) != RQ_OK || loop_count < 1 || max_ctx < 0) return 0;
   const rq::SplitPlan p = rq::plan_splits(*s, loop_count, max_ctx);
-  return size_t(rq::kWsHeaderBytes) +
+  return size_t(rq::kWsHeaderBytes) + rq::ws_ticket_bytes(*s, loop_count) +
          size_t(s->batch) * s->n_q_heads * loop_count * p.n_splits * rq::partial_floats(*s) *
              sizeof(float);
 }

@@ -91,4 +91,66 @@ __device__ __forceinline__ int k_row_offset(int k, int bits, int ng) {
   return ((w % bits) * ng + w / bits) * 4 + (k & 3);
 }
 
+// Split combine of one query column by one warp: merge the split partial records (m, l, two
+// pad floats, acc_ref[D], acc_res[D]), add the current token's BF16 K/V (kp, vp rows, or
+// null), undo the rotation of the residual accumulator (R^T y = signs * (H y) / sqrt(d);
+// signs of the column's kv-head, or null when there is no residual part), store bf16.
+// `failed` (a split gave up) makes the output NaN.
+template <int D>
+__device__ __forceinline__ void combine_column(const float* part, int n_splits, const uint16_t* qp,
+                                               const uint16_t* kpp, const uint16_t* vpp,
+                                               const int8_t* sg, float scale_log2, bool failed,
+                                               uint16_t* o, int lane) {
+  constexpr int P = D / 32;
+  constexpr int rec = 4 + 2 * D;
+  float M = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, part[s * rec]);
+  float ps = -INFINITY;
+  float vp[P];
+  if (kpp) {
+    float dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      vp[j] = bf16_bits_to_float(vpp[lane * P + j]);
+      dot = fmaf(bf16_bits_to_float(qp[lane * P + j]) * scale_log2,
+                 bf16_bits_to_float(kpp[lane * P + j]), dot);
+    }
+    ps = warp_sum(dot);
+    M = fmaxf(M, ps);
+  }
+  float ar[P], ae[P];
+#pragma unroll
+  for (int j = 0; j < P; ++j) ar[j] = ae[j] = 0.f;
+  float ell = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < n_splits; ++s) {
+      const float ms = part[s * rec];
+      if (ms == -INFINITY) continue;
+      const float f = exp2f(ms - M);
+      ell += f * part[s * rec + 1];
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        ar[j] = fmaf(f, part[s * rec + 4 + lane * P + j], ar[j]);
+        ae[j] = fmaf(f, part[s * rec + 4 + D + lane * P + j], ae[j]);
+      }
+    }
+    if (kpp) {
+      const float f = exp2f(ps - M);
+      ell += f;
+#pragma unroll
+      for (int j = 0; j < P; ++j) ar[j] = fmaf(f, vp[j], ar[j]);
+    }
+  }
+  if (sg) {
+    warp_fwht<P>(ae, lane);
+    const float inv_sqrt_d = (D == 128) ? 0.08838834764831845f : 0.125f;
+#pragma unroll
+    for (int j = 0; j < P; ++j) ar[j] = fmaf(ae[j] * inv_sqrt_d, float(sg[lane * P + j]), ar[j]);
+  }
+  float inv = ell > 0.f ? 1.f / ell : 0.f;
+  if (failed) inv = __int_as_float(0x7fc00000);
+#pragma unroll
+  for (int j = 0; j < P; ++j) o[lane * P + j] = float_to_bf16_bits(ar[j] * inv);
+}
+
 }  // namespace rq

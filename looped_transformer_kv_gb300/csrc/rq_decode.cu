@@ -26,7 +26,6 @@ __global__ void __launch_bounds__(128) combine_kernel(const int8_t* __restrict__
                                                       uint16_t* __restrict__ out, int B, int Hq,
                                                       int H, int loop_count, int n_splits,
                                                       float scale_log2) {
-  constexpr int P = D / 32;
   const int lane = threadIdx.x & 31;
   const int64_t wid = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (wid >= int64_t(B) * Hq * loop_count) return;
@@ -34,64 +33,13 @@ __global__ void __launch_bounds__(128) combine_kernel(const int8_t* __restrict__
   const int hq = int((wid / loop_count) % Hq);
   const int b = int(wid / (int64_t(loop_count) * Hq));
   const int h = hq / (Hq / H);
-  const int rec = int(partial_floats_d(D));
-  const float* part = ws + wid * n_splits * rec;
-
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, part[s * rec]);
-  float ps = -INFINITY;
-  float kp[P], vp[P];
-  if (pending) {
-    const uint16_t* qp = q + wid * D + lane * P;
-    const uint16_t* kpp = pending + ((int64_t(b) * 2 + 0) * loop_count + li) * H * D +
-                          int64_t(h) * D + lane * P;
-    const uint16_t* vpp = pending + ((int64_t(b) * 2 + 1) * loop_count + li) * H * D +
-                          int64_t(h) * D + lane * P;
-    float dot = 0.f;
-#pragma unroll
-    for (int j = 0; j < P; ++j) {
-      kp[j] = bf16_bits_to_float(kpp[j]);
-      vp[j] = bf16_bits_to_float(vpp[j]);
-      dot = fmaf(bf16_bits_to_float(qp[j]) * scale_log2, kp[j], dot);
-    }
-    ps = warp_sum(dot);
-    M = fmaxf(M, ps);
-  }
-  float ar[P], ae[P];
-#pragma unroll
-  for (int j = 0; j < P; ++j) ar[j] = ae[j] = 0.f;
-  float ell = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const float ms = part[s * rec];
-      if (ms == -INFINITY) continue;
-      const float f = exp2f(ms - M);
-      ell += f * part[s * rec + 1];
-#pragma unroll
-      for (int j = 0; j < P; ++j) {
-        ar[j] = fmaf(f, part[s * rec + 4 + lane * P + j], ar[j]);
-        ae[j] = fmaf(f, part[s * rec + 4 + D + lane * P + j], ae[j]);
-      }
-    }
-    if (pending) {
-      const float f = exp2f(ps - M);
-      ell += f;
-#pragma unroll
-      for (int j = 0; j < P; ++j) ar[j] = fmaf(f, vp[j], ar[j]);
-    }
-  }
-  if (v_signs) {  // R^T y = signs * (H y) / sqrt(d)
-    warp_fwht<P>(ae, lane);
-    const int8_t* sg = v_signs + int64_t(h) * D + lane * P;
-    const float inv_sqrt_d = (D == 128) ? 0.08838834764831845f : 0.125f;
-#pragma unroll
-    for (int j = 0; j < P; ++j) ar[j] = fmaf(ae[j] * inv_sqrt_d, float(sg[j]), ar[j]);
-  }
-  float inv = ell > 0.f ? 1.f / ell : 0.f;
-  if (err && *err) inv = __int_as_float(0x7fc00000);  // a split kernel gave up: NaN output
-  uint16_t* o = out + wid * D + lane * P;
-#pragma unroll
-  for (int j = 0; j < P; ++j) o[j] = float_to_bf16_bits(ar[j] * inv);
+  const uint16_t* kpp = pending ? pending + ((int64_t(b) * 2 + 0) * loop_count + li) * H * D + int64_t(h) * D
+                                : nullptr;
+  const uint16_t* vpp = pending ? pending + ((int64_t(b) * 2 + 1) * loop_count + li) * H * D + int64_t(h) * D
+                                : nullptr;
+  combine_column<D>(ws + wid * n_splits * int64_t(partial_floats_d(D)), n_splits, q + wid * D, kpp, vpp,
+                    v_signs ? v_signs + int64_t(h) * D : nullptr, scale_log2, err && *err,
+                    out + wid * D, lane);
 }
 
 }  // namespace
@@ -149,12 +97,15 @@ cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const rq_
                              cudaStream_t stream) {
   const SplitPlan plan = plan_splits_rq(s, loop_begin, loop_count, max_ctx);
   unsigned* err = reinterpret_cast<unsigned*>(ws);
-  float* part = ws + kWsHeaderBytes / sizeof(float);
-  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream);
+  const size_t tb = ws_ticket_bytes(s, loop_count);
+  unsigned* tickets = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + kWsHeaderBytes);
+  float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + kWsHeaderBytes + tb);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeaderBytes + tb, stream);   // error word, tickets
   if (e != cudaSuccess) return e;
   e = launch_rq_decode_mma(s, cache, paging, q, loop_begin, loop_count, ctx_lens, plan.n_splits,
-                           plan.tokens_per_split, part, err, stream);
+                           plan.tokens_per_split, pending, out, part, tickets, err, stream);
   if (e != cudaSuccess) return e;
+  if (decode_combines_in_kernel(s, loop_begin, loop_count)) return cudaSuccess;
   return launch_combine(s, cache.rot_signs[1], q, loop_count, pending, plan.n_splits, out, part,
                         err, stream);
 }

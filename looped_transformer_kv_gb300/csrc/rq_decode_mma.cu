@@ -151,6 +151,20 @@ int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* 
   return n;
 }
 
+bool decode_combines_in_kernel(const rq_shape& s, int loop_begin, int loop_count) {
+  QueryBlock blocks[64];
+  const int nb = plan_query_blocks(s.n_q_heads / s.n_kv_heads, loop_begin, loop_count, s.n_loops,
+                                   blocks, 64);
+  if (nb < 1) return false;
+  for (int i = 0; i < nb; ++i) {
+    const int nr = blocks[i].nr;
+    bool res4 = false;
+    for (int ri = 0; ri < nr; ++ri) res4 |= s.res_bits[blocks[i].r0 + ri] == 4;
+    if (block_packing(blocks[i]) != 2 || !has_single_column_variant(s.head_dim, res4, nr)) return false;
+  }
+  return true;
+}
+
 SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int max_ctx) {
   // the resident CTAs per SM follow the largest shared-memory block of the call
   QueryBlock blocks[64];
@@ -171,7 +185,8 @@ SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int 
 cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
                                  const uint16_t* q, int loop_begin, int loop_count,
                                  const int32_t* ctx_lens, int n_splits, int tokens_per_split,
-                                 float* part, unsigned* err, cudaStream_t stream) {
+                                 const uint16_t* pending, uint16_t* out, float* part,
+                                 unsigned* tickets, unsigned* err, cudaStream_t stream) {
   cudaError_t e = prepare_kernels();
   if (e != cudaSuccess) return e;
   QueryBlock blocks[64];
@@ -192,6 +207,10 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.ctx_lens = ctx_lens;
     a.part = part;
     a.err = err;
+    a.pending = pending;
+    a.out = out;
+    a.vsigns = cache.rot_signs[1];
+    a.tickets = tickets + int64_t(bi) * s.batch * s.n_kv_heads;   // this block's tickets
     a.B = s.batch;
     a.Hq = s.n_q_heads;
     a.H = s.n_kv_heads;

@@ -67,6 +67,10 @@ struct MmaArgs {
   const int32_t* ctx_lens;
   float* part;
   unsigned* err;
+  const uint16_t* pending;   // current token's K/V rows, or null
+  uint16_t* out;
+  const int8_t* vsigns;      // V rotation signs [H][D]
+  unsigned* tickets;         // [B][H] of this launch's block: splits stored
   int B, Hq, H, L, cap, g, loop_begin, loop_count, n_splits, tokens_per_split;
   QueryBlock blk;
   float scale_log2;
@@ -245,8 +249,43 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   auto o_krc = [&](int ri) { return FIXED ? F_RES + ri * F_RS : a.off_krc[ri]; };
   auto o_vrc = [&](int ri) { return FIXED ? F_RES + ri * F_RS + F_VRC : a.off_vrc[ri]; };
 
+  // Single-column blocks combine their splits in the kernel: the last split of this
+  // (sequence, kv-head) to store its records merges every split's records, adds the current
+  // token and undoes the rotation (the stores of the other splits are ordered before their
+  // ticket by a fence, and the ticket before the reads).  Other blocks leave that to the
+  // combine kernel: for them the fence at every CTA's end and the combine on the tail cost
+  // more than the launch it saves.
+  auto combine_if_last = [&]() {
+    if constexpr (!SC) return;
+    __syncthreads();
+    bool last = false;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      last = atomicAdd(&a.tickets[int64_t(b) * a.H + h], 1u) == unsigned(a.n_splits - 1);
+    }
+    if (!__syncthreads_or(last)) return;
+    __threadfence();
+    const bool gave_up = *reinterpret_cast<volatile const unsigned*>(a.err) != 0u;
+    constexpr int rec = int(partial_floats_d(D));
+    for (int col = warp; col < NQ; col += kW) {
+      const int li = col / blk.gw, gi = blk.gi0 + col % blk.gw;
+      if (li >= blk.nl || gi >= a.g) continue;
+      const int lc = blk.lb + li - a.loop_begin;
+      const int64_t wid = (int64_t(b) * a.Hq + int64_t(h) * a.g + gi) * a.loop_count + lc;
+      const uint16_t* kpp = nullptr;
+      const uint16_t* vpp = nullptr;
+      if (a.pending) {
+        kpp = a.pending + ((int64_t(b) * 2 + 0) * a.loop_count + lc) * a.H * D + int64_t(h) * D;
+        vpp = a.pending + ((int64_t(b) * 2 + 1) * a.loop_count + lc) * a.H * D + int64_t(h) * D;
+      }
+      combine_column<D>(a.part + wid * a.n_splits * rec, a.n_splits, a.q + wid * D, kpp, vpp,
+                        a.vsigns + int64_t(h) * D, a.scale_log2, gave_up, a.out + wid * D, lane);
+    }
+  };
+
   if (FIXED && SB != a.stage_bytes) {   // host and kernel disagree on the layout: refuse
     if (threadIdx.x == 0) atomicOr(a.err, 1u);
+    combine_if_last();                  // (NaN outputs)
     return;
   }
   const SmemLayout lay = smem_layout(D, RES4, a.n_stages, SB, a.n_pg);
@@ -1012,14 +1051,15 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   }
 
   if (__syncthreads_or(failed)) {
-    // a copy never completed: flag it, wait (bounded) for the copies still in flight, leave
+    // a copy never completed: flag it, wait (bounded) for the copies still in flight, and
+    // take the ticket without records (the combine's output is NaN)
     if (threadIdx.x == 0) {
       atomicOr(a.err, 1u);
       const int issued = int(cnt[kIssuedSlot]);
       for (int t = issued - S < 0 ? 0 : issued - S; t < issued; ++t)
         mbar_wait_bounded(smem_u32(&bars[t % S]), uint32_t((t / S) & 1), kWaitLimitNs);
     }
-    __syncthreads();
+    combine_if_last();
     return;
   }
 
@@ -1161,7 +1201,18 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
     }
     *reinterpret_cast<float4*>(o + 4 + 4 * q4) = v;
   }
+  combine_if_last();
 }
+
+}  // namespace
+
+// Single-column packing exists for head dim 128 and one loop (the final one, or one residual
+// loop of 2 or 4 bits).
+inline bool has_single_column_variant(int D, bool res4, int nr) {
+  return D == 128 && (res4 ? nr == 1 : nr <= 1);
+}
+
+namespace {
 
 template <int D, bool PG, int PK>
 KernelFn pick_generic(bool res4) {
@@ -1176,9 +1227,9 @@ KernelFn pick_generic(bool res4) {
 template <bool PG, int PK>
 KernelFn pick_pg(int D, bool res4, int nr) {
   if constexpr (PK == 2) {
-    if (D == 128 && !res4 && nr == 0) return rq_mma_kernel<128, false, 0, PG, 2>;
-    if (D == 128 && !res4 && nr == 1) return rq_mma_kernel<128, false, 1, PG, 2>;
-    if (D == 128 && res4 && nr == 1) return rq_mma_kernel<128, true, 1, PG, 2>;
+    if (has_single_column_variant(D, res4, nr))
+      return nr == 0 ? rq_mma_kernel<128, false, 0, PG, 2>
+                     : (res4 ? rq_mma_kernel<128, true, 1, PG, 2> : rq_mma_kernel<128, false, 1, PG, 2>);
     return pick_pg<PG, 1>(D, res4, nr);
   } else {
     if (D == 128 && !res4) {

@@ -11,6 +11,15 @@ namespace rq {
 constexpr int kMaxResPerBlock = 8;   // residual loops handled by one decode launch
 constexpr int kWsHeaderBytes = 256;  // workspace header: uint32 error word, then padding
 
+// Packed-cache decode workspace: header, then one uint32 ticket per (sequence, kv-head, query
+// block) counting the splits that have stored their partial records (the last one combines),
+// then the partial records.  Header and tickets are cleared by every call.
+inline size_t ws_ticket_bytes(const rq_shape& s, int loop_count) {
+  // blocks per kv-head <= query heads per kv-head x loops in the call
+  const size_t n = size_t(s.batch) * s.n_q_heads * (loop_count > 0 ? loop_count : 1);
+  return (n * 4 + 255) / 256 * 256;
+}
+
 // A block of query columns handled by one launch: query heads [gi0, gi0 + gw) of each
 // kv-head (gw a power of two <= 8) for loops [lb, lb + nl); residual loops [r0, r0 + nr).
 struct QueryBlock {
@@ -52,10 +61,14 @@ __host__ __device__ constexpr size_t partial_floats_d(int D) { return size_t(4 +
 
 int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* out, int max_out);
 
+// Split kernel launches of a decode call.  Single-column blocks: the last split of each
+// (sequence, kv-head) combines into `out` (tickets: the call's cleared ticket region).
+bool decode_combines_in_kernel(const rq_shape& s, int loop_begin, int loop_count);
 cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
                                  const uint16_t* q, int loop_begin, int loop_count,
                                  const int32_t* ctx_lens, int n_splits, int tokens_per_split,
-                                 float* part, unsigned* err, cudaStream_t stream);
+                                 const uint16_t* pending, uint16_t* out, float* part,
+                                 unsigned* tickets, unsigned* err, cudaStream_t stream);
 
 struct SplitPlan {
   int n_splits;          // split-KV partitions of the context

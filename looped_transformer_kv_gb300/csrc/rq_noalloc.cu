@@ -50,8 +50,8 @@ extern "C" rq_status rq_decode_attention_noalloc(const rq_shape* shape, const rq
   void* ws = nullptr;
   const rq_status st = scratch_for_current_device(&ws);
   if (st != RQ_OK) return st;
-  // the scratch array's error word is cleared by the call itself; every partial record the
-  // combine reads is rewritten by the split kernel, so nothing else needs clearing
+  // the scratch array's error word and tickets are cleared by the call itself; every partial
+  // record the combine reads is rewritten by the split kernels, so nothing else needs clearing
   return rq_decode_attention(shape, cache, q, loop_begin, loop_count, pending_kv, ctx_lens,
                              max_ctx, out, ws, kNoAllocScratchBytes, stream);
 }
