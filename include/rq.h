@@ -130,7 +130,9 @@ size_t rq_decode_workspace_bytes(const rq_shape* shape, int32_t loop_count, int3
  *   out        bf16 [B][Hq][loop_count][d].  A row with no cached and no pending token
  *              is written as zeros.
  *   ws         device workspace of at least rq_decode_workspace_bytes(...) bytes,
- *              256-byte aligned.
+ *              256-byte aligned.  The call clears its head (error word, split tickets) on
+ *              the stream and then fills the split records; calls that share a workspace
+ *              must not overlap on the GPU.
  * Loop-l queries attend over loop l's rebuilt K/V; scores are scaled by softmax_scale. */
 rq_status rq_decode_attention(const rq_shape* shape, const rq_cache* cache,
                               const uint16_t* q, int32_t loop_begin, int32_t loop_count,
