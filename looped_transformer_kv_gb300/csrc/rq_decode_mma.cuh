@@ -483,6 +483,36 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   }
   __syncthreads();   // fragments and sums visible to every warp
 
+  // Offset terms of the scores, sum_g z_g,t sum(q_g), as one m16n8k8 MMA per reference or
+  // residual loop and tile: A = the (step, offset) fp16 words of a token's 4 groups as stored,
+  // B = 0 against the steps and the column's group sums against the offsets (scaled by 2^19,
+  // which bounds them by 2^14 given the fragment scale, as fp16 high and low parts).  B slots:
+  // 0/1 reference high/low, 2 + 2 ri / 3 + 2 ri residual loop ri (masked to its columns);
+  // with the 4-column packing the low parts sit in columns 4-7 of the even slots.  Used for
+  // blocks of at most one residual loop: with more, the added live registers cost spills
+  // that outweigh the saved instructions.
+  constexpr bool OFS = !SC && NRT >= 0 && NRT <= 1;
+  constexpr float kOfsScale = 524288.f, kOfsUnscale = 1.f / 524288.f;
+  const uint32_t* OB = reinterpret_cast<const uint32_t*>(smem + lay.ob);
+  if constexpr (OFS) {
+    uint32_t* ob = reinterpret_cast<uint32_t*>(smem + lay.ob);
+    for (int i = threadIdx.x; i < 8 * 32; i += kW * 32) {
+      const int j = i >> 5, rr = (i & 31) >> 2, cc = i & 3;
+      const int slot = j >> 1;             // 0: reference, 1 + ri: residual loop ri
+      const bool low = HL ? rr >= 4 : (j & 1) != 0;
+      const int col = HL ? (rr & 3) : rr;
+      float v = 0.f;
+      if (cc < NG && !(HL && (j & 1)) &&
+          (slot == 0 || (slot - 1 < (NRT > 3 ? 3 : NRT) && col_ri(col) == slot - 1)))
+        v = (slot == 0 ? Qsum : QRsum)[cc * NQ + col] * kOfsScale;
+      __half hi, lw;
+      split_half(v, hi, lw);
+      ob[i] = uint32_t(__half_as_ushort(low ? lw : hi)) << 16;
+    }
+    __syncthreads();
+  }
+  const int cw = c < NG ? c : 0;   // this lane's group in the offset MMAs' A operand
+
   // columns of this lane: score/value-accumulator fragments hold columns 2c and 2c + 1, the
   // value B operand column r
   int riD[2], krmD[2], kaD[2], vaD[2], vrmD[2];
@@ -631,6 +661,29 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
         float R[4], E[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) R[k] = E[k] = 0.f;
+        if constexpr (OFS) {   // the offset terms: one MMA per loop (two without packing)
+          uint32_t w0 = lds32(sb + o_km + (tr0 * NG + cw) * 4);
+          uint32_t w1 = lds32(sb + o_km + (tr1 * NG + cw) * 4);
+          if (NG < 4 && c >= NG) w0 = w1 = 0u;
+          mma_f16_k8(R, w0, w1, OB[lane]);
+          if (!HL) mma_f16_k8(R, w0, w1, OB[32 + lane]);
+          if constexpr (PER_LOOP) {
+#pragma unroll
+            for (int ri = 0; ri < (PER_LOOP ? NRT : 1); ++ri) {
+              const int ob0 = FIXED ? F_RES + ri * F_RS + F_KRM : a.off_krm[ri];
+              uint32_t v0w = lds32(sb + ob0 + (tr0 * NG + cw) * 4);
+              uint32_t v1w = lds32(sb + ob0 + (tr1 * NG + cw) * 4);
+              if (NG < 4 && c >= NG) v0w = v1w = 0u;
+              mma_f16_k8(E, v0w, v1w, OB[(2 + 2 * ri) * 32 + lane]);
+              if (!HL) mma_f16_k8(E, v0w, v1w, OB[(3 + 2 * ri) * 32 + lane]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            R[k] *= kOfsUnscale;
+            E[k] *= kOfsUnscale;
+          }
+        }
         uint32_t km0[NG], km1[NG], kw0[NG], kw1[NG];
         load_words<NG>(sb + o_km + tr0 * NG * 4, km0);
         load_words<NG>(sb + o_km + tr1 * NG * 4, km1);
@@ -656,11 +709,18 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
               }
             }
             const float2 m0 = meta_f2(km0[gq]), m1 = meta_f2(km1[gq]);
-            const float2 qs = *reinterpret_cast<const float2*>(&Qsum[gq * NQ + 2 * c]);
-            R[0] = fmaf(m0.x, Dg[0], fmaf(m0.y, qs.x, R[0]));
-            R[1] = fmaf(m0.x, Dg[1], fmaf(m0.y, qs.y, R[1]));
-            R[2] = fmaf(m1.x, Dg[2], fmaf(m1.y, qs.x, R[2]));
-            R[3] = fmaf(m1.x, Dg[3], fmaf(m1.y, qs.y, R[3]));
+            if constexpr (OFS) {   // offsets: above
+              R[0] = fmaf(m0.x, Dg[0], R[0]);
+              R[1] = fmaf(m0.x, Dg[1], R[1]);
+              R[2] = fmaf(m1.x, Dg[2], R[2]);
+              R[3] = fmaf(m1.x, Dg[3], R[3]);
+            } else {
+              const float2 qs = *reinterpret_cast<const float2*>(&Qsum[gq * NQ + 2 * c]);
+              R[0] = fmaf(m0.x, Dg[0], fmaf(m0.y, qs.x, R[0]));
+              R[1] = fmaf(m0.x, Dg[1], fmaf(m0.y, qs.y, R[1]));
+              R[2] = fmaf(m1.x, Dg[2], fmaf(m1.y, qs.x, R[2]));
+              R[3] = fmaf(m1.x, Dg[3], fmaf(m1.y, qs.y, R[3]));
+            }
           }
           if (nr > 0) {  // residuals of every loop of the block
             float dsel[4];
@@ -747,9 +807,14 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
             for (int e = 0; e < 2; ++e) {
               const float2 m0 = ld_meta(sb + krmD[e] + (tr0 * NG + gq) * 4);
               const float2 m1 = ld_meta(sb + krmD[e] + (tr1 * NG + gq) * 4);
-              const float qrs = QRsum[gq * NQ + 2 * c + e];
-              E[e] = fmaf(m0.x, dsel[e], fmaf(m0.y, qrs, E[e]));
-              E[2 + e] = fmaf(m1.x, dsel[2 + e], fmaf(m1.y, qrs, E[2 + e]));
+              if constexpr (OFS && PER_LOOP) {   // offsets: above
+                E[e] = fmaf(m0.x, dsel[e], E[e]);
+                E[2 + e] = fmaf(m1.x, dsel[2 + e], E[2 + e]);
+              } else {
+                const float qrs = QRsum[gq * NQ + 2 * c + e];
+                E[e] = fmaf(m0.x, dsel[e], fmaf(m0.y, qrs, E[e]));
+                E[2 + e] = fmaf(m1.x, dsel[2 + e], fmaf(m1.y, qrs, E[2 + e]));
+              }
             }
           }
         }

@@ -29,7 +29,7 @@ struct QueryBlock {
 // Shared-memory layout of the tensor-core decode kernel (byte offsets).  The stage region
 // also holds the four warps' partial accumulators when the tiles are done.
 struct SmemLayout {
-  int qf, qr2, qr4, qsum, qrsum, red, cnt, pg, bars, total;
+  int qf, qr2, qr4, qsum, qrsum, ob, red, cnt, pg, bars, total;
 };
 
 // page_ids: physical page ids of a split's tiles kept for a paged cache (0 otherwise).
@@ -47,6 +47,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, 
   s.qr4 = o;   o += res4 ? frag : 0;
   s.qsum = o;  o += NG * NQ * 4;
   s.qrsum = o; o += NG * NQ * 4;
+  s.ob = o;    o += 8 * 32 * 4;       // B fragments of the score offset MMAs
   s.red = o;   o += 2 * W * NQ * 4;
   s.cnt = o;   o += 16 * 4;           // stage release counters, tiles issued
   s.pg = o;    o += page_ids * 4;
