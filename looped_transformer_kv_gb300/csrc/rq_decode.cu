@@ -102,10 +102,12 @@ cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const rq_
   float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + kWsHeaderBytes + tb);
   cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeaderBytes + tb, stream);   // error word, tickets
   if (e != cudaSuccess) return e;
+  const bool in_kernel = decode_combines_in_kernel(s, loop_begin, loop_count);
   e = launch_rq_decode_mma(s, cache, paging, q, loop_begin, loop_count, ctx_lens, plan.n_splits,
-                           plan.tokens_per_split, pending, out, part, tickets, err, stream);
+                           plan.tokens_per_split, pending, out, part, in_kernel ? tickets : nullptr,
+                           err, stream);
   if (e != cudaSuccess) return e;
-  if (decode_combines_in_kernel(s, loop_begin, loop_count)) return cudaSuccess;
+  if (in_kernel) return cudaSuccess;
   return launch_combine(s, cache.rot_signs[1], q, loop_count, pending, plan.n_splits, out, part,
                         err, stream);
 }

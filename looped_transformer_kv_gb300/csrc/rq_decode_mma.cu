@@ -121,9 +121,16 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
 // loops) measured slower on GB300 because of the lower occupancy.
 constexpr int kMaxBlockColumns = kNQ;
 
-int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* out, int max_out) {
+int plan_query_blocks(const rq_shape& s, int loop_begin, int loop_count, QueryBlock* out,
+                      int max_out) {
+  const int g = s.n_q_heads / s.n_kv_heads, L = s.n_loops;
   int gw = 1;
   while (gw < g && gw < 8) gw <<= 1;
+  // One query head per kv-head and head dim 128: a 4-bit residual loop takes a single-column
+  // block of its own, the other loops of the call share blocks.  (The multi-column variants
+  // with a 4-bit loop hold more registers than three CTAs per SM allow without spilling; the
+  // second read of the reference tile costs less.)
+  const bool four_alone = gw == 1 && s.head_dim == 128;
   int n = 0;
   for (int gi0 = 0; gi0 < g; gi0 += gw) {
     int l = loop_begin;
@@ -136,9 +143,12 @@ int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* 
       int nl = 0, nres = 0;
       while (l + nl < lend && (nl + 1) * gw <= kMaxBlockColumns) {
         const bool res = (l + nl) != L - 1;
+        const bool four = res && s.res_bits[l + nl] == 4;
         if (res && nres == kMaxResPerBlock) break;
+        if (four_alone && four && nl > 0) break;     // ends the block before it
         nres += res;
         ++nl;
+        if (four_alone && four) break;               // and stands alone
       }
       bq.nl = nl;
       bq.r0 = l;
@@ -153,8 +163,7 @@ int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* 
 
 bool decode_combines_in_kernel(const rq_shape& s, int loop_begin, int loop_count) {
   QueryBlock blocks[64];
-  const int nb = plan_query_blocks(s.n_q_heads / s.n_kv_heads, loop_begin, loop_count, s.n_loops,
-                                   blocks, 64);
+  const int nb = plan_query_blocks(s, loop_begin, loop_count, blocks, 64);
   if (nb < 1) return false;
   for (int i = 0; i < nb; ++i) {
     const int nr = blocks[i].nr;
@@ -168,8 +177,7 @@ bool decode_combines_in_kernel(const rq_shape& s, int loop_begin, int loop_count
 SplitPlan plan_splits_rq(const rq_shape& s, int loop_begin, int loop_count, int max_ctx) {
   // the resident CTAs per SM follow the largest shared-memory block of the call
   QueryBlock blocks[64];
-  const int g = s.n_q_heads / s.n_kv_heads;
-  const int nb = plan_query_blocks(g, loop_begin, loop_count, s.n_loops, blocks, 64);
+  const int nb = plan_query_blocks(s, loop_begin, loop_count, blocks, 64);
   rq_cache dummy;
   memset(&dummy, 0, sizeof(dummy));
   int ctas = 0;
@@ -191,7 +199,7 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
   if (e != cudaSuccess) return e;
   QueryBlock blocks[64];
   const int g = s.n_q_heads / s.n_kv_heads;
-  const int nb = plan_query_blocks(g, loop_begin, loop_count, s.n_loops, blocks, 64);
+  const int nb = plan_query_blocks(s, loop_begin, loop_count, blocks, 64);
   if (nb < 0) return cudaErrorInvalidConfiguration;
   const float scale = s.softmax_scale > 0.f ? s.softmax_scale : 1.0f / sqrtf(float(s.head_dim));
   for (int bi = 0; bi < nb; ++bi) {
@@ -210,7 +218,7 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.pending = pending;
     a.out = out;
     a.vsigns = cache.rot_signs[1];
-    a.tickets = tickets + int64_t(bi) * s.batch * s.n_kv_heads;   // this block's tickets
+    a.tickets = tickets ? tickets + int64_t(bi) * s.batch * s.n_kv_heads : nullptr;   // block's
     a.B = s.batch;
     a.Hq = s.n_q_heads;
     a.H = s.n_kv_heads;

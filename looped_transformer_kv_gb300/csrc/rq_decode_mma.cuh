@@ -70,7 +70,8 @@ struct MmaArgs {
   const uint16_t* pending;   // current token's K/V rows, or null
   uint16_t* out;
   const int8_t* vsigns;      // V rotation signs [H][D]
-  unsigned* tickets;         // [B][H] of this launch's block: splits stored
+  unsigned* tickets;         // [B][H] of this launch's block: splits stored (or null: the
+                             // combine kernel merges the splits)
   int B, Hq, H, L, cap, g, loop_begin, loop_count, n_splits, tokens_per_split;
   QueryBlock blk;
   float scale_log2;
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   // more than the launch it saves.
   auto combine_if_last = [&]() {
     if constexpr (!SC) return;
+    if (!a.tickets) return;   // (a call with other blocks: the combine kernel merges)
     __syncthreads();
     bool last = false;
     if (threadIdx.x == 0) {

@@ -60,10 +60,13 @@ __host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, 
 // Split partial record: m, l, two pad floats, acc_ref[D], acc_res[D] (16-byte aligned rows).
 __host__ __device__ constexpr size_t partial_floats_d(int D) { return size_t(4 + 2 * D); }
 
-int plan_query_blocks(int g, int loop_begin, int loop_count, int L, QueryBlock* out, int max_out);
+int plan_query_blocks(const rq_shape& s, int loop_begin, int loop_count, QueryBlock* out,
+                      int max_out);
 
-// Split kernel launches of a decode call.  Single-column blocks: the last split of each
-// (sequence, kv-head) combines into `out` (tickets: the call's cleared ticket region).
+// Split kernel launches of a decode call.  When every block of the call is single-column
+// (decode_combines_in_kernel), the last split of each (sequence, kv-head) combines into `out`
+// (tickets: the call's cleared ticket region); otherwise tickets is null and the combine
+// kernel follows.
 bool decode_combines_in_kernel(const rq_shape& s, int loop_begin, int loop_count);
 cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
                                  const uint16_t* q, int loop_begin, int loop_count,
