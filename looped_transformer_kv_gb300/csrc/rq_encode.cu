@@ -49,16 +49,23 @@ __device__ __forceinline__ void quantize_lane(const float (&v)[P], int (&c)[P], 
   z_bits = float_to_half_bits(mn);
   const float s_h = half_bits_to_float(s_bits);
   const float z_h = half_bits_to_float(z_bits);
+  // (x - z) / s correctly rounded from the correctly rounded reciprocal y of s: q = RN(n y),
+  // then one correction RN(q + RN(n - q s) y) (Markstein's quotient correction, which gives
+  // the correctly rounded quotient when y is the correctly rounded 1/s); s is an fp16 value
+  // > 0 and n is bounded, so no intermediate leaves the normal fp32 range
+  const float y = s_h > 0.0f ? __frcp_rn(s_h) : 0.0f;
 #pragma unroll
   for (int j = 0; j < P; ++j) {
-    int code = 0;
+    float qv = 0.0f;
     if (s_h > 0.0f) {
-      float qv = rintf(__fdiv_rn(__fsub_rn(v[j], z_h), s_h));
+      const float n = __fsub_rn(v[j], z_h);
+      const float q0 = __fmul_rn(n, y);
+      const float rem = __fmaf_rn(-q0, s_h, n);
+      qv = rintf(__fmaf_rn(rem, y, q0));
       qv = fminf(fmaxf(qv, 0.0f), float(LEVELS));
-      code = int(qv);
     }
-    c[j] = code;
-    deq[j] = fmaf(float(code), s_h, z_h);
+    c[j] = int(qv);
+    deq[j] = fmaf(qv, s_h, z_h);
   }
 }
 
