@@ -43,10 +43,11 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Walsh-Hadamard transform (Sylvester order, unnormalised) of a d-vector spread over a
-// warp: lane holds channels [lane*P, lane*P + P), P = d / 32 in {2, 4}.  Channel index
-// bits below log2(P) are butterflied in registers, the rest across lanes.
-template <int P>
+// Walsh-Hadamard transform (Sylvester order, unnormalised) of a d-vector spread over LANES
+// lanes (a warp, or each half of it): lane i of the group holds channels [i*P, i*P + P),
+// P = d / LANES.  Channel index bits below log2(P) are butterflied in registers, the rest
+// across lanes, lowest bit first.
+template <int P, int LANES = 32>
 __device__ __forceinline__ void warp_fwht(float (&v)[P], int lane) {
 #pragma unroll
   for (int h = 1; h < P; h <<= 1) {
@@ -60,7 +61,7 @@ __device__ __forceinline__ void warp_fwht(float (&v)[P], int lane) {
     }
   }
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
+  for (int m = 1; m < LANES; m <<= 1) {
 #pragma unroll
     for (int j = 0; j < P; ++j) {
       float u = __shfl_xor_sync(RQ_FULL_MASK, v[j], m);

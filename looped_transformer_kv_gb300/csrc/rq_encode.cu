@@ -1,7 +1,10 @@
 // ResidualQuant encode: runs once the token's final loop has finished (deferred write,
-// rit.work summary "How each pass's KV cache is reconstructed").  One warp encodes one
+// rit.work summary "How each pass's KV cache is reconstructed").  VL lanes encode one
 // (sequence, new token, kv-head, K/V): the final loop's state becomes the INT4 reference,
-// every other loop a least-squares-scaled, Hadamard-rotated 2- or 4-bit residual.
+// every other loop a least-squares-scaled, Hadamard-rotated 2- or 4-bit residual.  Large
+// calls (bulk prefill) put K and V of a token in the two halves of a warp (VL 16: fewer
+// shuffle stages and instructions per vector); small ones (the per-step append) give a
+// vector a whole warp (VL 32: the shortest dependency chain per vector).
 #include "rq_common.cuh"
 #include "rq_kernels.h"
 
@@ -19,7 +22,16 @@ struct EncodeArgs {
   int8_t res_bits[RQ_MAX_LOOPS];
   const int32_t* bt;     // block table of a paged cache, or null
   int32_t max_pages, n_pages;
+  int32_t vec;           // kv_new rows allow one vector load of a lane's channels
 };
+
+// Sum over the VL lanes of a vector.
+template <int VL>
+__device__ __forceinline__ float vec_sum(float v) {
+#pragma unroll
+  for (int o = VL / 2; o > 0; o >>= 1) v += __shfl_xor_sync(RQ_FULL_MASK, v, o);
+  return v;
+}
 
 // Group min / max over the lanes that share a 32-channel group (LPG lanes).
 template <int LPG>
@@ -69,48 +81,52 @@ __device__ __forceinline__ void quantize_lane(const float (&v)[P], int (&c)[P], 
   }
 }
 
-// Store the packed bits of this lane's P channels.  BITS*P bits per lane: 4 (d 64, 2-bit),
-// 8 or 16.  Row byte k = lane's byte index; V rows go to the token-pair layout.
-template <int P, int BITS>
+// Store the packed bits of the P channels of lane `lane` (of the vector's lanes), the
+// natural row's bytes [lane * BITS * P / 8, ...): 8, 16 or 32 bits per lane.  K rows are
+// group-interleaved (NG groups of 32 channels); V rows go to the token-pair layout.
+template <int P, int BITS, int NG>
 __device__ __forceinline__ void store_codes(uint8_t* slot, int64_t tok, int row_bytes, bool is_v,
                                             const int (&c)[P], int lane) {
-  // d = 32 P channels, so the number of 32-channel groups is P
   uint32_t w = 0;
 #pragma unroll
   for (int j = 0; j < P; ++j) w |= uint32_t(c[j]) << (BITS * j);
   constexpr int LANE_BITS = BITS * P;
-  if (LANE_BITS == 4) {
-    uint32_t other = __shfl_down_sync(RQ_FULL_MASK, w, 1);
-    if ((lane & 1) == 0) {
-      const int k = lane >> 1;
-      uint8_t byte = uint8_t(w | (other << 4));
-      int64_t off = is_v ? vpair_offset(tok, k, row_bytes)
-                         : tok * row_bytes + k_row_offset(k, BITS, P);
-      slot[off] = byte;
-    }
-  } else if (LANE_BITS == 8) {
+  static_assert(LANE_BITS == 8 || LANE_BITS == 16 || LANE_BITS == 32, "lane bits");
+  if constexpr (LANE_BITS == 8) {
     const int k = lane;
     int64_t off = is_v ? vpair_offset(tok, k, row_bytes)
-                       : tok * row_bytes + k_row_offset(k, BITS, P);
+                       : tok * row_bytes + k_row_offset(k, BITS, NG);
     slot[off] = uint8_t(w);
-  } else {  // 16 bits: one aligned 16-bit unit
+  } else if constexpr (LANE_BITS == 16) {  // one aligned 16-bit unit
     const int k = 2 * lane;
     int64_t off = is_v ? vpair_offset(tok, k, row_bytes)
-                       : tok * row_bytes + k_row_offset(k, BITS, P);
+                       : tok * row_bytes + k_row_offset(k, BITS, NG);
     *reinterpret_cast<uint16_t*>(slot + off) = uint16_t(w);
+  } else {  // 32 bits: one K word, or two 16-bit units of a V token pair
+    const int k = 4 * lane;
+    if (is_v) {
+      *reinterpret_cast<uint16_t*>(slot + vpair_offset(tok, k, row_bytes)) = uint16_t(w);
+      *reinterpret_cast<uint16_t*>(slot + vpair_offset(tok, k + 2, row_bytes)) = uint16_t(w >> 16);
+    } else {
+      *reinterpret_cast<uint32_t*>(slot + tok * row_bytes + k_row_offset(k, BITS, NG)) = w;
+    }
   }
 }
 
-template <int D>
+template <int D, int VL>
 __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
-  constexpr int P = D / 32;   // channels per lane
-  constexpr int LPG = kGroup / P;
+  constexpr int P = D / VL;         // channels per lane
+  constexpr int LPG = kGroup / P;   // lanes per 32-channel group
   constexpr int NG = D / kGroup;
   const int lane = threadIdx.x & 31;
-  const int64_t wid = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int hl = lane & (VL - 1);   // lane within the vector
+  // vectors (sequence, token, kv-head, K/V), K/V fastest: a warp's halves (VL 16) hold the
+  // K and V states of one token and kv-head
+  const int64_t vid = (int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * (32 / VL) +
+                      lane / VL;
   const int64_t total = int64_t(a.B) * a.n_new * a.H * 2;
-  if (wid >= total) return;
-  int64_t r = wid;
+  if (vid >= total) return;
+  int64_t r = vid;
   const int kv = int(r % 2); r /= 2;
   const int h = int(r % a.H); r /= a.H;
   const int j = int(r % a.n_new); r /= a.n_new;
@@ -133,12 +149,33 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
   }
 
   const uint16_t* src = a.kv_new + int64_t(b) * a.sb + int64_t(j) * a.st + int64_t(kv) * a.skv +
-                        int64_t(h) * a.sh + lane * P;
+                        int64_t(h) * a.sh + hl * P;
   const int L = a.L;
   auto load = [&](int l, float (&v)[P]) {
     const uint16_t* p = src + int64_t(l) * a.sl;
+    uint16_t e[P];
+    if (a.vec) {   // one 16-byte (P 8) or 8-byte (P 4) load
+      if constexpr (P == 8) {
+        const uint4 w = *reinterpret_cast<const uint4*>(p);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int q = 0; q < P; ++q) v[q] = bf16_bits_to_float(p[q]);
+        for (int q = 0; q < 4; ++q) {
+          e[2 * q] = uint16_t(u[q]);
+          e[2 * q + 1] = uint16_t(u[q] >> 16);
+        }
+      } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(p);
+        e[0] = uint16_t(w.x);
+        e[1] = uint16_t(w.x >> 16);
+        e[2] = uint16_t(w.y);
+        e[3] = uint16_t(w.y >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < P; ++q) e[q] = p[q];
+    }
+#pragma unroll
+    for (int q = 0; q < P; ++q) v[q] = bf16_bits_to_float(e[q]);
   };
 
   // ---- reference: the final loop, INT4 ----
@@ -149,9 +186,9 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
   quantize_lane<P, 15>(x_ref, c, ref_hat, s_bits, z_bits);
   {
     uint8_t* codes = a.cache.ref_codes[kv] + base * (D / 2);
-    store_codes<P, 4>(codes, tok, D / 2, is_v, c, lane);
-    if (lane % LPG == 0) {
-      const int g = lane / LPG;
+    store_codes<P, 4, NG>(codes, tok, D / 2, is_v, c, hl);
+    if (hl % LPG == 0) {
+      const int g = hl / LPG;
       uint16_t* meta = a.cache.ref_meta[kv] + (base + tok) * (2 * NG) + 2 * g;
       *reinterpret_cast<uint32_t*>(meta) = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
     }
@@ -160,11 +197,11 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
   float den = 0.f;
 #pragma unroll
   for (int q = 0; q < P; ++q) den = fmaf(ref_hat[q], ref_hat[q], den);
-  den = warp_sum(den);
+  den = vec_sum<VL>(den);
 
   float sgn[P];
   {
-    const int8_t* sp = a.cache.rot_signs[kv] + int64_t(h) * D + lane * P;
+    const int8_t* sp = a.cache.rot_signs[kv] + int64_t(h) * D + hl * P;
 #pragma unroll
     for (int q = 0; q < P; ++q) sgn[q] = float(sp[q]);
   }
@@ -177,16 +214,16 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
     float num = 0.f;
 #pragma unroll
     for (int q = 0; q < P; ++q) num = fmaf(x[q], ref_hat[q], num);
-    num = warp_sum(num);
+    num = vec_sum<VL>(num);
     const float alpha = den > 0.f ? __fdiv_rn(num, den) : 0.f;
     const uint16_t a_bits = float_to_half_bits(alpha);
     const float a_h = half_bits_to_float(a_bits);
-    if (lane == 0) a.cache.alpha[kv][l][base + tok] = a_bits;
+    if (hl == 0) a.cache.alpha[kv][l][base + tok] = a_bits;
     // residual, rotation R r = H (signs * r) / sqrt(d)
     float y[P];
 #pragma unroll
     for (int q = 0; q < P; ++q) y[q] = fmaf(-a_h, ref_hat[q], x[q]) * sgn[q];
-    warp_fwht<P>(y, lane);
+    warp_fwht<P, VL>(y, hl);
 #pragma unroll
     for (int q = 0; q < P; ++q) y[q] *= inv_sqrt_d;
     float deq[P];
@@ -195,13 +232,13 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
     uint8_t* codes = a.cache.res_codes[kv][l] + base * row;
     if (bits == 2) {
       quantize_lane<P, 3>(y, c, deq, s_bits, z_bits);
-      store_codes<P, 2>(codes, tok, row, is_v, c, lane);
+      store_codes<P, 2, NG>(codes, tok, row, is_v, c, hl);
     } else {
       quantize_lane<P, 15>(y, c, deq, s_bits, z_bits);
-      store_codes<P, 4>(codes, tok, row, is_v, c, lane);
+      store_codes<P, 4, NG>(codes, tok, row, is_v, c, hl);
     }
-    if (lane % LPG == 0) {
-      const int g = lane / LPG;
+    if (hl % LPG == 0) {
+      const int g = hl / LPG;
       uint16_t* meta = a.cache.res_meta[kv][l] + (base + tok) * (2 * NG) + 2 * g;
       *reinterpret_cast<uint32_t*>(meta) = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
     }
@@ -233,13 +270,24 @@ cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const rq_pag
   a.bt = paging ? paging->block_table : nullptr;
   a.max_pages = paging ? paging->max_pages : 0;
   a.n_pages = paging ? paging->n_pages : 0;
-  const int64_t warps = int64_t(s.batch) * n_new * s.n_kv_heads * 2;
+  // vectors of the call; below a few per SM, a vector of d 128 gets a whole warp
+  const int64_t vectors = int64_t(s.batch) * n_new * s.n_kv_heads * 2;
+  const int vl = (s.head_dim == 128 && vectors < 64 * 152) ? 32 : 16;
+  // one vector load per lane (its P consecutive channels) where kv_new allows it
+  const int p = s.head_dim / vl;
+  a.vec = p >= 4 && reinterpret_cast<uintptr_t>(kv_new) % (2 * p) == 0;
+  for (int k = 0; k < 5; ++k) a.vec = a.vec && (strides[k] % p == 0);
+  const int64_t warps = (vectors * vl + 31) / 32;
   const int64_t blocks = (warps + 3) / 4;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (s.head_dim == 128)
-    encode_kernel<128><<<unsigned(blocks), 128, 0, stream>>>(a);
-  else
-    encode_kernel<64><<<unsigned(blocks), 128, 0, stream>>>(a);
+  if (s.head_dim == 128) {
+    if (vl == 32)
+      encode_kernel<128, 32><<<unsigned(blocks), 128, 0, stream>>>(a);
+    else
+      encode_kernel<128, 16><<<unsigned(blocks), 128, 0, stream>>>(a);
+  } else {
+    encode_kernel<64, 16><<<unsigned(blocks), 128, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
