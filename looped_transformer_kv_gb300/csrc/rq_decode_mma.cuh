@@ -29,8 +29,8 @@
 // (values: exact normal fp16 code times a power of two removed per output row at the end).
 // The other operand (queries, softmax weights) is split into an fp16 high part and an fp16
 // low part (two MMAs; for blocks of at most 4 query columns one MMA, the low parts riding in
-// the 4 free columns) and so carries about 22 significant bits; products are exact in the
-// fp32 accumulators.
+// the 4 free columns; for a single query column the columns carry its channel groups) and so
+// carries about 22 significant bits; products are exact in the fp32 accumulators.
 // Query columns of every loop share the fragments: the residual codes of loop l meet the
 // query fragments of every column, and each column keeps only its own loop's dot product
 // (a per-loop score accumulator, or a query fragment masked to the loop's columns); in the
