@@ -110,9 +110,12 @@ rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache,
                            void* stream);
 
 /* Workspace bytes needed by rq_decode_attention / rq_bf16_decode_attention for this
- * shape, loop_count and max_ctx on the current device: a 256-byte header followed by the
- * split-KV partials.  After rq_decode_attention completes, the header's first uint32 is 0;
- * it is nonzero if a pipeline wait inside the kernel gave up (outputs are then NaN). */
+ * shape, loop_count and max_ctx on the current device: a 256-byte header, the split
+ * tickets, then the split-KV partials.  After rq_decode_attention completes, the header's
+ * first uint32 is 0; it is nonzero if a pipeline wait inside the kernel gave up or a paged
+ * call met a bad table entry.  The outputs of every (sequence, kv-head) whose splits met the
+ * fault are then NaN; calls that merge their splits in a separate combine make all outputs
+ * NaN.  A caller checks the word, not the outputs. */
 size_t rq_decode_workspace_bytes(const rq_shape* shape, int32_t loop_count, int32_t max_ctx);
 
 /* Fused decode attention over the packed cache (rit.work summary, "How each pass's KV
@@ -162,7 +165,7 @@ rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k,
  * block_table[b * max_pages + j].  shape->capacity must equal 64 * max_pages (the logical
  * capacity of a sequence).  The table is read on the device: an entry outside
  * [0, n_pages) is never dereferenced -- the encode skips that token, the decode reads page 0
- * instead and flags the workspace error word (outputs NaN). */
+ * instead and flags the workspace error word (the affected outputs NaN). */
 typedef struct {
   const int32_t* block_table;  /* device int32 [B][max_pages]                         */
   int32_t max_pages;           /* table columns: logical pages per sequence            */

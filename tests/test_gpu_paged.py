@@ -111,3 +111,29 @@ def test_paged_table_entry_out_of_range_is_flagged_not_read():
     p1 = int(table[0, 1])
     for x, y in zip(before, after):
         assert torch.equal(x[p1].view(torch.uint8), y[p1].view(torch.uint8))
+
+
+def test_bad_table_entry_in_single_column_calls_gives_nan():
+    # one query head per kv-head and head dim 128: the per-loop calls run the single-column
+    # variants, which merge their splits in the split kernel; the error word is set and every
+    # output of the sequence whose split met the bad entry is NaN (the other sequence's units
+    # may have merged before the flag)
+    cfg = _cfg("layer_1p4b", batch=2, n_q_heads=2, n_kv_heads=2)
+    w = Workload(cfg, capacity=512, ctx_lens=[450, 300], batch=2)
+    pc, paging, bt, table = _paged_twin(w, spare_pages=0, seed=11)
+    good = w.out_buffer(1), w.workspace(1)
+    q = w.q[:, :, 0:1].contiguous()
+    pend = w.pending[:, :, 0:1].contiguous()
+    rqm.rq.paged_decode_attention(w.shape, pc, paging, q, 0, 1, pend, w.ctx_lens, w.max_ctx,
+                                  good[0], good[1])
+    torch.cuda.synchronize()
+    assert good[1][:1].view(torch.int32).item() == 0
+    assert torch.isfinite(good[0].float()).all()
+    bad = bt.clone()
+    bad[1, 2] = -3                                  # sequence 1, page 2: out of range
+    o, ws = w.out_buffer(1), w.workspace(1)
+    rqm.rq.paged_decode_attention(w.shape, pc, rqm.rq.make_paging(bad, pc.n_pages), q, 0, 1, pend,
+                                  w.ctx_lens, w.max_ctx, o, ws)
+    torch.cuda.synchronize()
+    assert ws[:1].view(torch.int32).item() != 0
+    assert torch.isnan(o[1].float()).all()
