@@ -96,13 +96,14 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
     a.off_va[ri] = off;  off += kT * 2;
   }
   a.stage_bytes = off;
+  a.qrm_bytes = masked_fragment_bytes(D, res4, bq.nr, block_packing(bq));
   a.blk = bq;
   a.n_pg = n_pg;
   bl.res4 = res4;
   // most resident CTAs per SM first (latency hiding), then the deepest pipeline
   int best_ctas = 0;
   for (int stages = 3; stages >= 2; --stages) {
-    const size_t sm = smem_layout(D, res4, stages, a.stage_bytes, n_pg).total;
+    const size_t sm = smem_layout(D, res4, stages, a.stage_bytes, n_pg, a.qrm_bytes).total;
     if (sm > 200 * 1024) continue;
     const int ctas = resident_ctas(D, res4, bq.nr, block_packing(bq), sm);
     if (ctas > best_ctas) {

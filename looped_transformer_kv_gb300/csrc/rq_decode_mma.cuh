@@ -76,6 +76,7 @@ struct MmaArgs {
   QueryBlock blk;
   float scale_log2;
   int n_stages, stage_bytes;
+  int qrm_bytes;             // masked rotated-query fragments (masked_fragment_bytes)
   const int32_t* bt;   // block table of a paged cache, or null
   int max_pages, n_pages, n_pg;   // table columns, physical pages, page-id slots in shared memory
   int off_kc, off_km, off_vc, off_vm;
@@ -224,6 +225,9 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   constexpr bool PER_LOOP = NRT >= 1 && NRT <= 3;   // one residual score accumulator per loop
   constexpr bool HL = PK >= 1;                      // low parts in columns 4-7
   constexpr bool SC = PK == 2;                      // one query column, groups in columns
+  // 4-column packing with 2 or 3 residual loops of 2 bits: each loop's residual MMAs take the
+  // rotated-query fragments masked to its columns (no per-loop accumulator to select from)
+  constexpr bool MASKB = PK == 1 && !RES4 && PER_LOOP && NRT >= 2;
   static_assert(!SC || (NRT == 0 || NRT == 1) && D == 128, "single-column blocks: D 128, one loop");
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -290,7 +294,13 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
     combine_if_last();                  // (NaN outputs)
     return;
   }
-  const SmemLayout lay = smem_layout(D, RES4, a.n_stages, SB, a.n_pg);
+  const int qrm_bytes = masked_fragment_bytes(D, RES4, NRT, PK);
+  if (a.qrm_bytes != qrm_bytes || (qrm_bytes > 0) != MASKB) {   // layouts disagree: refuse
+    if (threadIdx.x == 0) atomicOr(a.err, 1u);
+    combine_if_last();
+    return;
+  }
+  const SmemLayout lay = smem_layout(D, RES4, a.n_stages, SB, a.n_pg, qrm_bytes);
   uint4* QF = reinterpret_cast<uint4*>(smem + lay.qf);
   uint4* QR2 = reinterpret_cast<uint4*>(smem + lay.qr2);
   uint4* QR4 = reinterpret_cast<uint4*>(smem + lay.qr4);
@@ -514,6 +524,17 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
     __syncthreads();
   }
   const int cw = c < NG ? c : 0;   // this lane's group in the offset MMAs' A operand
+  // masked fragments: [ri][k-step][lane], the rotated-query fragment where the lane's column
+  // (high or low part of query column (lane / 4) & 3) is residual loop ri's, else zero
+  uint2* QRM = reinterpret_cast<uint2*>(smem + lay.qrm);
+  if constexpr (MASKB) {
+    for (int i = threadIdx.x; i < NRT * NG * 2 * 32; i += kW * 32) {
+      const int ri = i / (NG * 2 * 32), rem = i % (NG * 2 * 32);
+      const uint2 v = *reinterpret_cast<const uint2*>(&QR2[rem]);
+      QRM[i] = col_ri(((rem & 31) >> 2) & 3) == ri ? v : make_uint2(0u, 0u);
+    }
+    __syncthreads();
+  }
 
   // columns of this lane: score/value-accumulator fragments hold columns 2c and 2c + 1, the
   // value B operand column r
@@ -754,7 +775,10 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
                     a_pairs_4bit(wh, s, a1, a3);
                   }
                   const int fi = (gq * 2 + s) * 32 + lane;
-                  if constexpr (HL) {
+                  if constexpr (MASKB) {   // into the one accumulator: other loops' columns get 0
+                    const uint2 bq = QRM[(ri * NG * 2 + gq * 2 + s) * 32 + lane];
+                    mma_f16(dsel, a0, a1, a2, a3, bq.x, bq.y);
+                  } else if constexpr (HL) {
                     const uint2 bq = *reinterpret_cast<const uint2*>((RES4 && !two) ? &QR4[fi] : &QR2[fi]);
                     mma_f16(Dr, a0, a1, a2, a3, bq.x, bq.y);
                   } else {
@@ -764,8 +788,10 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
                   }
                 }
                 // each column keeps its own loop's product
+                if constexpr (!MASKB) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) dsel[k] = blend(loop_mask[k & 1][ri], Dr[k], dsel[k]);
+                  for (int k = 0; k < 4; ++k) dsel[k] = blend(loop_mask[k & 1][ri], Dr[k], dsel[k]);
+                }
               }
             } else {
               // run-time loop count: one accumulator, query fragments masked to each loop's

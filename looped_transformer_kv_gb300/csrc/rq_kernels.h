@@ -11,6 +11,15 @@ namespace rq {
 constexpr int kMaxResPerBlock = 8;   // residual loops handled by one decode launch
 constexpr int kWsHeaderBytes = 256;  // workspace header: uint32 error word, then padding
 
+// Variants of the decode kernel that keep, per residual loop, the rotated-query fragments
+// masked to the loop's columns (4-column packing, 2-bit residual loops, residual-loop count
+// fixed at compile time and >= 2): bytes of that region, else 0.  Kernel and host use this
+// one rule.
+__host__ __device__ inline int masked_fragment_bytes(int D, bool res4, int nr, int pk) {
+  const bool fixed = (D == 128 && (nr == 2 || nr == 3)) || (D == 64 && nr == 3);
+  return (pk == 1 && !res4 && fixed) ? nr * (D / 32) * 2 * 32 * 8 : 0;
+}
+
 // Packed-cache decode workspace: header, then one uint32 ticket per (sequence, kv-head, query
 // block) counting the splits that have stored their partial records (the last one combines),
 // then the partial records.  Header and tickets are cleared by every call.
@@ -29,12 +38,14 @@ struct QueryBlock {
 // Shared-memory layout of the tensor-core decode kernel (byte offsets).  The stage region
 // also holds the four warps' partial accumulators when the tiles are done.
 struct SmemLayout {
-  int qf, qr2, qr4, qsum, qrsum, ob, red, cnt, pg, bars, total;
+  int qf, qr2, qr4, qrm, qsum, qrsum, ob, red, cnt, pg, bars, total;
 };
 
-// page_ids: physical page ids of a split's tiles kept for a paged cache (0 otherwise).
+// page_ids: physical page ids of a split's tiles kept for a paged cache (0 otherwise);
+// qrm_bytes: the rotated-query fragments masked per residual loop (0 if the variant keeps
+// none).
 __host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, int stage_bytes,
-                                                  int page_ids) {
+                                                  int page_ids, int qrm_bytes) {
   const int NG = D / 32, NQ = 8, W = 4;
   SmemLayout s;
   int o = stages * stage_bytes;
@@ -45,6 +56,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, 
   s.qf = o;    o += frag;
   s.qr2 = o;   o += frag;
   s.qr4 = o;   o += res4 ? frag : 0;
+  s.qrm = o;   o += qrm_bytes;
   s.qsum = o;  o += NG * NQ * 4;
   s.qrsum = o; o += NG * NQ * 4;
   s.ob = o;    o += 8 * 32 * 4;       // B fragments of the score offset MMAs
