@@ -501,9 +501,9 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   // which bounds them by 2^14 given the fragment scale, as fp16 high and low parts).  B slots:
   // 0/1 reference high/low, 2 + 2 ri / 3 + 2 ri residual loop ri (masked to its columns);
   // with the 4-column packing the low parts sit in columns 4-7 of the even slots.  Used for
-  // blocks of at most one residual loop: with more, the added live registers cost spills
-  // that outweigh the saved instructions.
-  constexpr bool OFS = !SC && NRT >= 0 && NRT <= 1;
+  // blocks of at most one residual loop and for 4-column blocks; 8-column blocks with more
+  // residual loops keep the per-element form (the added live registers cost spills there).
+  constexpr bool OFS = !SC && NRT >= 0 && (NRT <= 1 || PK == 1);
   constexpr float kOfsScale = 524288.f, kOfsUnscale = 1.f / 524288.f;
   const uint32_t* OB = reinterpret_cast<const uint32_t*>(smem + lay.ob);
   if constexpr (OFS) {
