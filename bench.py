@@ -36,7 +36,7 @@ KERNEL_SOURCES = ("looped_transformer_kv_gb300/csrc/rq_decode_mma.cu",
                   "looped_transformer_kv_gb300/csrc/rq_common.cuh",
                   "looped_transformer_kv_gb300/csrc/rq_kernels.h")
 TRAFFIC = {
-    ("79290b9ddba51873", "layer_1p4b"): 484631040 + 11278336,  # profiles/rq_mma_kernel_layer_1p4b.md
+    ("7a5789489900c373", "layer_1p4b"): 483010304 + 11158272,  # profiles/rq_mma_kernel_layer_1p4b.md
 }
 
 
