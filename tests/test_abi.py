@@ -106,3 +106,17 @@ def test_paging_arguments_are_validated(lib):
                                     st, None, 0, 1, None) == 1
     assert L.rq_paged_cache_bytes(ctypes.byref(s), 0) == 0
     assert L.rq_paged_cache_bytes(ctypes.byref(s), 8) == O.cache_bytes(128, 4, (2, 2, 2), 64, 2, 8)
+
+
+@pytest.mark.parametrize("lc,ctx", [(1, 4096), (4, 4096), (2, 1), (4, 0)])
+def test_decode_workspace_is_header_tickets_and_split_records(lib, lc, ctx):
+    # header (256 B: error word), one uint32 ticket per (sequence, query head, loop) rounded to
+    # 256 B, then n_splits partial records (m, l, 2 pads, acc_ref[d], acc_res[d]) per column
+    s = _shape(lib, capacity=4096)
+    ws = lib.lib().rq_decode_workspace_bytes(ctypes.byref(s), lc, ctx)
+    cols = 2 * 4 * lc
+    tickets = -(-cols * 4 // 256) * 256
+    rec = (4 + 2 * 128) * 4
+    rest = ws - 256 - tickets
+    assert rest > 0 and rest % (cols * rec) == 0, (ws, rest)
+    assert rest // (cols * rec) <= max(1, -(-ctx // 64))      # at most one split per 64-token tile
