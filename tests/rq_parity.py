@@ -3,18 +3,28 @@
 Encode parity is conditional (GPU arithmetic is fp32, the oracle's fp64): for every stored
 fp16 value (step, offset, a_l) and every code, the oracle recomputes the value; where the
 GPU's value differs, it is accepted only if the two are neighbours and the oracle's
-pre-rounding value lies within 1e-6 (relative to the value for fp16 quantities, in code
-units for codes) of the boundary between them.  The oracle then continues with the GPU's
-choice.  Everything else must match bit for bit, packed bytes included.  Reported counts:
-codes whose value lies within the band (`band`, out of `codes`; exact half-way ties, which
-both sides round to even, included) and elements where the GPU's neighbouring choice was
-taken (`followed`, out of `elements`), which must stay below 1e-5 of all elements.
+pre-rounding value lies within 1e-6 of the rounding boundary between them (relative to the
+value for fp16 quantities; relative to the spacing of the boundaries, i.e. in code units,
+for codes).  The oracle then continues with the GPU's choice.  Everything else must match
+bit for bit, packed bytes included.
+
+Counted separately for packed codes and for fp16 values:
+  ties       the fp64 pre-rounding value lies exactly on a boundary (a code quotient of
+             k + 1/2, an fp16 midpoint): both sides round it to even, so it cannot differ;
+  near       the value lies within the band but not exactly on the boundary: the elements
+             where fp32 and fp64 arithmetic could take different neighbours;
+  followed   elements where the GPU did take the other neighbour.
+The near-boundary criterion is on packed codes: code `near` < 1e-5 of all codes.  For fp16
+values the band (1e-6 relative around midpoints 2^-10 relative apart) holds about 0.2% of any
+generic quantity whatever computes it, so there the bound is on the choices actually taken:
+`followed` (codes and fp16 values) < 1e-5 of all elements.
 
 Output parity: GPU bf16 output vs the oracle's fp64 output,
     max over elements of (|gpu - ref| - ulp_bf16(ref)/2) <= 2e-3,
     mean over elements of max(0, |gpu - ref| - ulp_bf16(ref)/2) <= 2e-4,
 i.e. the error budget is for the arithmetic, on top of the unavoidable rounding of the
-result to bf16.
+result to bf16.  Also reported: the fraction of outputs not equal to bf16_rne(ref) and the
+fraction more than one bf16 ulp away from it.
 """
 
 import numpy as np
@@ -41,7 +51,10 @@ class Follow:
         self.gpu = gpu
         self.total = 0
         self.codes = 0         # packed codes checked
-        self.band = 0          # codes whose pre-rounding value lies within the band
+        self.ties = 0          # codes: pre-rounding quotient exactly k + 1/2 (both round to even)
+        self.near = 0          # codes: within the band, not exactly on the boundary
+        self.f16_ties = 0      # fp16 values exactly on a midpoint
+        self.f16_near = 0      # fp16 values within the band, not on the midpoint
         self.followed = 0      # elements where the GPU's neighbouring choice was taken
         self.bad = 0           # any other disagreement
         self.bad_names = {}
@@ -52,16 +65,22 @@ class Follow:
         rounded = np.asarray(rounded, dtype=np.float64)
         diff = g != rounded
         if name.endswith("_c"):
-            band = np.abs(pre - (np.floor(pre) + 0.5)) <= CODE_BAND
+            dist = np.abs(pre - (np.floor(pre) + 0.5))      # to the nearest boundary
+            in_band = dist <= CODE_BAND
             near = diff & (np.abs(g - rounded) == 1) & \
                 (np.abs(pre - (g + rounded) / 2) <= CODE_BAND)
             self.codes += rounded.size
-            self.band += int(band.sum())
+            self.ties += int((in_band & (dist == 0)).sum())
+            self.near += int((in_band & (dist > 0)).sum())
         else:
+            dist = np.abs(pre - _fp16_neighbour_mid(pre, rounded))   # boundary on pre's side
+            in_band = dist <= REL_BAND * np.abs(pre)
             toward = np.where(g > rounded, np.float16(np.inf), np.float16(-np.inf))
             adjacent = np.nextafter(rounded.astype(np.float16),
                                     toward.astype(np.float16)).astype(np.float64) == g
             near = diff & adjacent & (np.abs(pre - (g + rounded) / 2) <= REL_BAND * np.abs(pre))
+            self.f16_ties += int((in_band & (dist == 0)).sum())
+            self.f16_near += int((in_band & (dist > 0)).sum())
         bad = diff & ~near
         self.total += rounded.size
         self.followed += int(near.sum())
@@ -132,26 +151,49 @@ def output_errors(gpu, ref):
     ref = np.asarray(ref, np.float64)
     err = np.abs(gpu - ref)
     excess = np.maximum(err - bf16_half_ulp(ref), 0.0)
+    # against the correctly rounded result: bf16_rne(ref) and one bf16 ulp at its magnitude
+    rne = O.bf16_round(ref)
+    ulp = 2.0 * bf16_half_ulp(rne)
+    off = np.abs(gpu - rne)
     return {"max_excess": float(excess.max(initial=0.0)), "mean_excess": float(excess.mean()),
-            "max_abs": float(err.max(initial=0.0)), "mean_abs": float(err.mean())}
+            "max_abs": float(err.max(initial=0.0)), "mean_abs": float(err.mean()),
+            "n": int(gpu.size), "not_rne": int(np.count_nonzero(off)),
+            "beyond_1ulp": int(np.count_nonzero(off > ulp))}
 
 
-def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True):
+def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True, cache=None,
+                states=None, ctx=None, pending_state=None):
     """Encode parity and output parity for sequence b, kv-head h of workload w.
 
     loop_calls: list of (loop_begin, loop_count); outs: matching GPU outputs (torch bf16
-    [B][Hq][loop_count][d]).  Returns a stats dict; raises AssertionError on a failure.
+    [B][Hq][loop_count][d]).  By default the slice's tokens are the generator's states at
+    positions 0..ctx-1 (ctx = w.ctx_list[b]) and the current token is the generator's state at
+    position ctx.  A caller whose cache holds other tokens (a serving run that appended
+    tokens) passes them: states [n][2][L][d] (n >= ctx: every stored token to check, the
+    first ctx of them attended), ctx, and pending_state [2][L][d].  cache: a paged twin
+    (PackedCache with n_pages) whose pages hold the slice, read through w's block table
+    argument instead of w's contiguous cache (cache=(paged_cache, table_numpy)).
+    Returns a stats dict; raises AssertionError on a failure.
     """
     cfg, d, L = w.cfg, w.d, w.L
     res_bits = list(cfg.res_bits[: L - 1])
-    ctx = w.ctx_list[b]
-    ntok = max(ctx, 1)
-    ntok_e = ntok + ntok % 2
-    x = synth.gen_states(cfg, w.layer, [b], np.arange(ntok_e), heads=[h])[0, :, :, :, 0, :]
+    ctx = w.ctx_list[b] if ctx is None else ctx
+    if states is None:
+        ntok = max(ctx, 1)
+        ntok_e = ntok + ntok % 2
+        x = synth.gen_states(cfg, w.layer, [b], np.arange(ntok_e), heads=[h])[0, :, :, :, 0, :]
+    else:
+        x = np.asarray(states)
+        ntok_e = x.shape[0]
+        assert ntok_e % 2 == 0 and ntok_e >= ctx
     x = x.astype(np.float64)                                      # [ntok][2][L][d]
-    sl = w.packed_slice(b, h, ntok_e)
+    if cache is None:
+        sl = w.packed_slice(b, h, ntok_e)
+    else:
+        sl = w.packed_slice_paged(cache[0], cache[1], b, h, ntok_e)
     signs = w.signs_np[h].astype(np.float64)                      # [2][d]
-    stats = {"elements": 0, "codes": 0, "band": 0, "followed": 0}
+    stats = {"elements": 0, "codes": 0, "ties": 0, "near": 0, "f16_ties": 0, "f16_near": 0,
+             "followed": 0}
     encs = []
     for kv in range(2):
         f = Follow(gpu_slice_to_oracle_names(sl, kv, d, L, res_bits))
@@ -161,11 +203,19 @@ def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True):
             assert packed_bytes_equal(enc, sl, kv, res_bits), "packed bytes differ kv=%d" % kv
         stats["elements"] += f.total
         stats["codes"] += f.codes
-        stats["band"] += f.band
+        stats["ties"] += f.ties
+        stats["near"] += f.near
+        stats["f16_ties"] += f.f16_ties
+        stats["f16_near"] += f.f16_near
         stats["followed"] += f.followed
         encs.append(enc_head(enc, ctx))
-    pend = synth.gen_states(cfg, w.layer, [b], [ctx], heads=[h])[0, 0, :, :, 0, :] \
-        .astype(np.float64) if pending else None                  # [2][L][d]
+    if not pending:
+        pend = None
+    elif pending_state is not None:
+        pend = np.asarray(pending_state, np.float64)              # [2][L][d]
+    else:
+        pend = synth.gen_states(cfg, w.layer, [b], [ctx], heads=[h])[0, 0, :, :, 0, :] \
+            .astype(np.float64)
     qall = synth.gen_queries(cfg, w.layer, [b])[0].astype(np.float64)   # [Hq][L][d]
     g = w.Hq // w.H
     errs = []
@@ -185,6 +235,9 @@ def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True):
     stats["mean_excess"] = float(np.mean([e["mean_excess"] for e in errs]))
     stats["max_abs"] = max(e["max_abs"] for e in errs)
     stats["mean_abs"] = float(np.mean([e["mean_abs"] for e in errs]))
+    stats["outputs"] = sum(e["n"] for e in errs)
+    stats["not_rne"] = sum(e["not_rne"] for e in errs)
+    stats["beyond_1ulp"] = sum(e["beyond_1ulp"] for e in errs)
     assert stats["max_excess"] <= MAX_ABS, stats
     assert stats["mean_excess"] <= MEAN_ABS, stats
     return stats

@@ -41,23 +41,31 @@ def test_full_size_sampled_slices(name):
     assert ws[:1].view(torch.int32).item() == 0 and ws1[:1].view(torch.int32).item() == 0
     rng = np.random.default_rng(17)
     samples = {(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))}
-    band = codes = followed = elements = 0
+    tot = dict(codes=0, elements=0, ties=0, near=0, f16_ties=0, f16_near=0, followed=0,
+               outputs=0, not_rne=0, beyond_1ulp=0)
     worst = {"max_excess": 0.0, "mean_excess": 0.0, "max_abs": 0.0, "mean_abs": 0.0}
     for b, h in sorted(samples):
         st = check_slice(w, b, h, calls, outs)
-        band += st["band"]
-        codes += st["codes"]
-        followed += st["followed"]
-        elements += st["elements"]
+        for k in tot:
+            tot[k] += st[k]
         for k in worst:
             worst[k] = max(worst[k], st[k])
-    # elements excused by the near-boundary rule (the GPU's neighbouring choice, within 1e-6
-    # of the boundary) stay under 1e-5 of all elements; `band` (codes within the band,
-    # exact half-way ties included, which both sides round to even) is reported only
-    print("%s: codes %d, in band %d, elements %d, neighbouring choices taken %d; output error "
-          "(worst slice) max excess %.3g, mean excess %.3g, max abs %.3g, mean abs %.3g"
-          % (name, codes, band, elements, followed, worst["max_excess"], worst["mean_excess"],
-             worst["max_abs"], worst["mean_abs"]))
-    assert followed < 1e-5 * elements, (followed, elements)
+    n_f16 = tot["elements"] - tot["codes"]
+    print("%s: codes %d: exact ties %d (%.2e), near-boundary not tied %d (%.2e); fp16 values %d: "
+          "in band %d (%.2e, ties %d); neighbouring choices taken %d (%.2e of %d elements); "
+          "outputs %d: not bf16_rne(oracle) %d (%.2e), more than 1 bf16 ulp from it %d; output "
+          "error (worst slice) max excess %.3g, mean excess %.3g, max abs %.3g, mean abs %.3g"
+          % (name, tot["codes"], tot["ties"], tot["ties"] / tot["codes"], tot["near"],
+             tot["near"] / tot["codes"], n_f16, tot["f16_near"] + tot["f16_ties"],
+             (tot["f16_near"] + tot["f16_ties"]) / n_f16, tot["f16_ties"], tot["followed"],
+             tot["followed"] / tot["elements"], tot["elements"], tot["outputs"], tot["not_rne"],
+             tot["not_rne"] / tot["outputs"], tot["beyond_1ulp"], worst["max_excess"],
+             worst["mean_excess"], worst["max_abs"], worst["mean_abs"]))
+    # packed codes: bit-exact apart from codes within 1e-6 of a rounding boundary (exact ties
+    # k + 1/2 excluded: both sides round them to even), whose count stays under 1e-5 of the codes
+    assert tot["near"] < 1e-5 * tot["codes"], tot
+    # every element where the GPU took the other neighbour (codes and fp16 values) is counted
+    # and stays under 1e-5 of all elements
+    assert tot["followed"] < 1e-5 * tot["elements"], tot
     del w
     torch.cuda.empty_cache()
