@@ -195,6 +195,20 @@ class Workload:
                                   self.ctx_lens, self.max_ctx, out, ws, stream)
 
     # ------------------------------------------------------------------ readback
+    def packed_slice_paged(self, pc, table, b, h, ntok):
+        """packed_slice of a paged cache `pc` whose block table is `table` (host [B][pages])."""
+        ntok += ntok % 2
+        out = {}
+        tb = table[b]
+        for kv in range(2):
+            out[("ref_codes", kv)] = _page_rows(pc.ref_codes[kv], tb, h, ntok).cpu().numpy()
+            out[("ref_meta", kv)] = _page_rows(pc.ref_meta[kv], tb, h, ntok).float().cpu().numpy()
+            for l in range(self.L - 1):
+                out[("res_codes", kv, l)] = _page_rows(pc.res_codes[kv][l], tb, h, ntok).cpu().numpy()
+                out[("res_meta", kv, l)] = _page_rows(pc.res_meta[kv][l], tb, h, ntok).float().cpu().numpy()
+                out[("alpha", kv, l)] = _page_rows(pc.alpha[kv][l], tb, h, ntok).float().cpu().numpy()
+        return out
+
     def packed_slice(self, b, h, ntok):
         """Host copies of the packed arrays of (sequence b, kv-head h), tokens [0, ntok)."""
         ntok += ntok % 2
@@ -210,6 +224,26 @@ class Workload:
         return out
 
 
+def _page_rows(arr, table_b, h, ntok):
+    """Rows [0, ntok) of one (sequence, kv-head) of a paged array [n_pages][Hkv][64][...],
+    following the sequence's block-table row `table_b` (host ints)."""
+    npg = -(-ntok // 64)
+    idx = torch.as_tensor(np.asarray(table_b[:npg], dtype=np.int64), device=arr.device)
+    rows = arr[idx, h]                                   # [npg][64][...]
+    return rows.reshape((npg * 64,) + tuple(rows.shape[2:]))[:ntok]
+
+
 def np_bf16(t):
     """bf16 torch tensor -> fp64 numpy."""
     return t.float().cpu().numpy().astype(np.float64)
+
+
+def budget_batches(cfg, budget_bytes, capacity):
+    """Fixed KV-memory budget for one layer: the largest batch whose packed cache fits
+    `budget_bytes`, and the largest whose BF16 cache ([B][Hkv][L][capacity][d], K and V) does.
+    Returns (rq_batch, bf16_batch, rq_bytes_per_sequence, bf16_bytes_per_sequence)."""
+    L, H, d = cfg.n_loops, cfg.n_kv_heads, cfg.head_dim
+    rq_seq = rq.cache_bytes(rq.make_shape(1, cfg.n_q_heads, H, d, L, capacity,
+                                          cfg.res_bits[: L - 1]))
+    bf_seq = 2 * H * L * capacity * d * 2
+    return int(budget_bytes // rq_seq), int(budget_bytes // bf_seq), int(rq_seq), int(bf_seq)

@@ -21,6 +21,8 @@ if torch.cuda.is_available():
     import looped_transformer_kv_gb300 as rqm
     from looped_transformer_kv_gb300.workload import Workload
 
+from rq_parity import check_slice  # noqa: E402
+
 
 def _cfg(name, **kw):
     return dataclasses.replace(synth.config_by_name(name), **kw)
@@ -71,6 +73,7 @@ def test_paged_cache_matches_contiguous(case):
     calls = [(0, cfg.n_loops)] + [(l, 1) for l in range(cfg.n_loops)]
     if cfg.n_loops > 2:
         calls.append((1, 2))
+    paged_outs = []
     for l0, lc in calls:
         o1, o2 = w.out_buffer(lc), w.out_buffer(lc)
         ws1, ws2 = w.workspace(lc), w.workspace(lc)
@@ -82,6 +85,11 @@ def test_paged_cache_matches_contiguous(case):
         torch.cuda.synchronize()
         assert ws2[:1].view(torch.int32).item() == 0
         assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)), (l0, lc)
+        paged_outs.append(o2)
+    # the paged cache's pages and the paged outputs against the oracle, every sequence
+    for b in range(w.B):
+        for h in sorted({0, w.H - 1}):
+            check_slice(w, b, h, calls, paged_outs, cache=(pc, table))
 
 
 def test_paged_table_entry_out_of_range_is_flagged_not_read():

@@ -1,11 +1,14 @@
 """Serving step under a CUDA graph: per-loop decode of every loop, deferred-write encode of
 the current token into slot ctx_len, ctx_len advanced on the device -- captured once and
 replayed token after token.  N replays must leave the cache and ctx_lens exactly as N eager
-steps do, and produce the same outputs bit for bit (the eager calls are checked against the
-fp64 oracle by test_gpu_parity.py)."""
+steps do, and produce the same outputs bit for bit.  The replayed run is also checked against
+the fp64 oracle on its own: the grown cache (ctx original tokens, then N appended copies of the
+current token) is re-encoded by the oracle and compared code for code, and the last step's
+per-loop outputs (ctx + N - 1 cached tokens plus the current token) are recomputed."""
 
 import dataclasses
 
+import numpy as np
 import pytest
 
 import synth
@@ -15,6 +18,8 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     from looped_transformer_kv_gb300.workload import Workload
+
+from rq_parity import check_slice  # noqa: E402
 
 
 def _arrays(cache):
@@ -59,3 +64,13 @@ def test_graph_replayed_serving_steps_match_eager_steps(name, over, ctx):
     for a, b in zip(outs["g"], outs["e"]):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert wss["g"][:1].view(torch.int32).item() == 0
+    # the replayed run against the oracle: each sequence's cache grew by `steps` copies of its
+    # current token (the deferred writes), and the last step attended over all but the last
+    calls = [(l, 1) for l in range(L)]
+    for b, c0 in enumerate(ctx):
+        n = c0 + steps
+        for h in sorted({0, w_graph.H - 1}):
+            x = synth.gen_states(cfg, 0, [b], np.arange(n + n % 2), heads=[h])[0, :, :, :, 0, :]
+            pend = synth.gen_states(cfg, 0, [b], [c0], heads=[h])[0, 0, :, :, 0, :]
+            x[c0:n] = pend
+            check_slice(w_graph, b, h, calls, outs["g"], states=x, ctx=n - 1, pending_state=pend)
