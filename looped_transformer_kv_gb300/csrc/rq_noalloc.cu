@@ -1,6 +1,6 @@
 // rq_decode_attention_noalloc: decode attention for callers that cannot allocate device
-// memory.  The split-KV scratch (error word + partial records) lives in one file-scope
-// device array instead of a caller-provided workspace.
+// memory.  The split-KV scratch (error word, split tickets, partial records) lives in one
+// file-scope device array instead of a caller-provided workspace.
 #include <mutex>
 
 #include "rq_common.cuh"
@@ -14,22 +14,29 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB, fixed at 
 static __device__ __align__(256) unsigned char g_rq_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices];   // device address of the array per device, once found
 
 // Device address of the scratch array on the current device.  In host code the array's
-// name is only a host-side stand-in, so the address is looked up once per device, with
-// that device current, and kept.
+// name is only a host-side stand-in, so the address is looked up with that device current.
+// Only a successful lookup is kept: a failed one (for example a first call made during
+// stream capture) is retried by the next call, and its error is cleared so that it does not
+// surface in a later, unrelated cudaGetLastError.
 rq_status scratch_for_current_device(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RQ_ERR_CUDA;
-  std::call_once(g_once[dev], [dev] {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return RQ_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_rq_scratch);
+    if (cudaGetSymbolAddress(&p, g_rq_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return RQ_ERR_CUDA;
+    }
     g_scratch_ptr[dev] = p;
-  });
-  if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return RQ_ERR_CUDA;
+  }
   *out = g_scratch_ptr[dev];
   return RQ_OK;
 }
@@ -43,10 +50,13 @@ extern "C" rq_status rq_decode_attention_noalloc(const rq_shape* shape, const rq
                                                  int32_t loop_count, const uint16_t* pending_kv,
                                                  const int32_t* ctx_lens, int32_t max_ctx,
                                                  uint16_t* out, void* stream) {
-  if (!shape) return RQ_ERR_INVALID_ARG;
-  const size_t need = rq_decode_workspace_bytes(shape, loop_count, max_ctx);
-  if (need == 0) return RQ_ERR_INVALID_ARG;          // invalid shape or loop range
-  if (need > kNoAllocScratchBytes) return RQ_ERR_WORKSPACE;
+  // the same checks, in the same order, as rq_decode_attention: same status for same arguments
+  const rq_status valid =
+      rq::validate_decode(shape, cache, q, loop_begin, loop_count, ctx_lens, max_ctx, out);
+  if (valid != RQ_OK) return valid;
+  // a valid call whose split-KV scratch would not fit the array: refused, nothing enqueued
+  if (rq_decode_workspace_bytes(shape, loop_count, max_ctx) > kNoAllocScratchBytes)
+    return RQ_ERR_WORKSPACE;
   void* ws = nullptr;
   const rq_status st = scratch_for_current_device(&ws);
   if (st != RQ_OK) return st;

@@ -120,3 +120,27 @@ def test_decode_workspace_is_header_tickets_and_split_records(lib, lc, ctx):
     rest = ws - 256 - tickets
     assert rest > 0 and rest % (cols * rec) == 0, (ws, rest)
     assert rest // (cols * rec) <= max(1, -(-ctx // 64))      # at most one split per 64-token tile
+
+
+@pytest.mark.parametrize("bad,max_ctx,status", [
+    (dict(head_dim=96), 64, 2), (dict(group=64), 64, 2), (dict(res_bits=(3, 2, 2)), 64, 2),
+    (dict(n_q_heads=3), 64, 1), ({}, 65, 1),                    # max_ctx above capacity
+    (dict(batch=4096, n_q_heads=64, n_kv_heads=64, n_loops=16, res_bits=(2,) * 15,
+          capacity=65536), 65537, 1),                           # large shape, max_ctx too big
+])
+def test_noalloc_entry_point_returns_the_workspace_entry_points_status(lib, bad, max_ctx, status):
+    # validation of the no-alloc call is the workspace call's, in the same order: an invalid
+    # call gets the same status from both, before any device is touched
+    L = lib.lib()
+    s = _shape(lib, **bad)
+    c = lib.RqCache()
+    for kv in range(2):                                         # non-null dummy arrays
+        c.ref_codes[kv] = c.ref_meta[kv] = c.rot_signs[kv] = 16
+        for l in range(16):
+            c.res_codes[kv][l] = c.res_meta[kv][l] = c.alpha[kv][l] = 16
+    p = ctypes.c_void_p(16)
+    ws_status = L.rq_decode_attention(ctypes.byref(s), ctypes.byref(c), p, 0, 1, None, p, max_ctx,
+                                      p, p, 1 << 40, None)
+    noalloc_status = L.rq_decode_attention_noalloc(ctypes.byref(s), ctypes.byref(c), p, 0, 1,
+                                                   None, p, max_ctx, p, None)
+    assert ws_status == noalloc_status == status

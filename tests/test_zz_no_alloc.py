@@ -1,7 +1,8 @@
 """rq_decode_attention_noalloc, the entry point for callers that cannot allocate device
 memory (a plug-in whose host framework owns all device memory, a C caller that must not
-allocate after start-up): it must give the same attention as rq_decode_attention with a
-caller-provided workspace, on consecutive calls that reuse its fixed scratch array.
+allocate after start-up): it must give the same attention, bit for bit, as
+rq_decode_attention with a caller-provided workspace (same kernels, same split plan), on
+consecutive calls that reuse its fixed scratch array.
 
 Collected last on purpose, so that a run stopping at its first failure has already run
 every other test."""
@@ -43,15 +44,21 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(name, over, ctx):
                                         w.ctx_lens, w.max_ctx, got)
             torch.cuda.synchronize()
             assert torch.isfinite(got.float()).all()
-            diff = (got.float() - want.float()).abs()
-            assert diff.max().item() <= 2e-3, diff.max().item()
+            # the same kernels with the same split plan: the same bits
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16)), \
+                (got.float() - want.float()).abs().max().item()
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
     # a shape whose split-KV scratch needs more than the fixed array: refused, nothing enqueued
     shape = rq.make_shape(4096, 64, 64, 128, 16, 65536, (2,) * 15)
     assert rq.decode_workspace_bytes(shape, 16, 65536) > rq.noalloc_scratch_bytes()
+    cache = rq._lib.RqCache()
+    for kv in range(2):                           # non-null dummies: the call must stop at the
+        cache.ref_codes[kv] = cache.ref_meta[kv] = cache.rot_signs[kv] = 16   # size check
+        for l in range(15):
+            cache.res_codes[kv][l] = cache.res_meta[kv][l] = cache.alpha[kv][l] = 16
+    p = rq.ctypes.c_void_p(16)
     status = rq._lib.lib().rq_decode_attention_noalloc(
-        rq.ctypes.byref(shape), rq.ctypes.byref(rq._lib.RqCache()), None, 0, 16, None, None,
-        65536, None, None)
+        rq.ctypes.byref(shape), rq.ctypes.byref(cache), p, 0, 16, None, p, 65536, p, None)
     assert status == 3                            # RQ_ERR_WORKSPACE
