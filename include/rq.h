@@ -112,8 +112,8 @@ rq_status rq_encode_append(const rq_shape* shape, const rq_cache* cache,
 /* Workspace bytes needed by rq_decode_attention / rq_bf16_decode_attention for this
  * shape, loop_count and max_ctx on the current device: a 256-byte header, the split
  * tickets, then the split-KV partials.  After rq_decode_attention completes, the header's
- * first uint32 is 0; it is nonzero if a pipeline wait inside the kernel gave up or a paged
- * call met a bad table entry.  The outputs of every (sequence, kv-head) whose splits met the
+ * first uint32 is 0; it is nonzero if a pipeline wait inside the kernel gave up, a paged
+ * call met a bad table entry or a ctx_len lay outside what the call covers.  The outputs of every (sequence, kv-head) whose splits met the
  * fault are then NaN; calls that merge their splits in a separate combine make all outputs
  * NaN.  A caller checks the word, not the outputs. */
 size_t rq_decode_workspace_bytes(const rq_shape* shape, int32_t loop_count, int32_t max_ctx);
@@ -129,7 +129,11 @@ size_t rq_decode_workspace_bytes(const rq_shape* shape, int32_t loop_count, int3
  *   pending_kv bf16 [B][2][loop_count][Hkv][d] (0 = K, 1 = V): the current token's BF16
  *              state of each loop in the call, attended after the cached tokens; or NULL.
  *   ctx_lens   device int32 [B]: cached tokens of each sequence (slots 0..ctx_len-1).
- *   max_ctx    host upper bound of ctx_lens (<= capacity); sizes the split-KV grid.
+ *   max_ctx    host upper bound of ctx_lens (<= capacity); sizes the split-KV grid.  A
+ *              device-side ctx_len above the tokens the grid covers (above max_ctx, as can
+ *              happen when a captured graph keeps a fixed max_ctx while ctx_lens advance),
+ *              above capacity or negative is not truncated silently: the workspace error
+ *              word is set and that sequence's outputs are NaN (see rq_decode_workspace_bytes).
  *   out        bf16 [B][Hq][loop_count][d].  A row with no cached and no pending token
  *              is written as zeros.
  *   ws         device workspace of at least rq_decode_workspace_bytes(...) bytes,

@@ -1,4 +1,4 @@
-"""ctypes declarations of librq's C ABI (include/rq.h, include/rq_synth.h).
+"""ctypes declarations of librq's C ABI (include/rq.h, include/rq_synth.h, include/rq_test.h).
 
 Loading fails loudly: there is no fallback implementation of any entry point.
 """
@@ -16,7 +16,8 @@ EXPORTS = ("rq_cache_bytes", "rq_encode_append", "rq_decode_workspace_bytes",
            "rq_decode_attention", "rq_bf16_decode_attention", "rq_status_str",
            "rq_synth_states", "rq_synth_queries", "rq_decode_noalloc_scratch_bytes",
            "rq_decode_attention_noalloc", "rq_paged_cache_bytes", "rq_paged_encode_append",
-           "rq_paged_decode_attention", "rq_advance_ctx")
+           "rq_paged_decode_attention", "rq_advance_ctx",
+           "rq_test_decode_attention_wait_runs_out")
 
 
 class RqShape(ctypes.Structure):
@@ -89,6 +90,9 @@ def lib():
     L.rq_paged_encode_append.restype = i32
     L.rq_paged_decode_attention.argtypes = [S, C, G, _P, i32, i32, _P, _P, i32, _P, _P, sz, _P]
     L.rq_paged_decode_attention.restype = i32
+    L.rq_test_decode_attention_wait_runs_out.argtypes = [S, C, _P, i32, i32, _P, _P, i32, _P,
+                                                         _P, sz, ctypes.c_uint64, _P]
+    L.rq_test_decode_attention_wait_runs_out.restype = i32
     L.rq_advance_ctx.argtypes = [_P, i32, i32, i32, _P]
     L.rq_advance_ctx.restype = i32
     L.rq_status_str.argtypes = [i32]

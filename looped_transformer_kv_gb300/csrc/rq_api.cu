@@ -3,6 +3,7 @@
 #include <cmath>
 #include <new>
 
+#include "../../include/rq_test.h"
 #include "rq_common.cuh"
 #include "rq_kernels.h"
 
@@ -44,15 +45,24 @@ rq_status check_cache(const rq_shape* s, const rq_cache* c) {
   return RQ_OK;
 }
 
-rq_status check_decode(const rq_shape* s, const uint16_t* q, int32_t loop_begin,
-                       int32_t loop_count, const int32_t* ctx_lens, int32_t max_ctx,
-                       uint16_t* out, void* ws, size_t ws_bytes) {
+// Decode arguments other than the workspace.
+rq_status check_decode_args(const rq_shape* s, const uint16_t* q, int32_t loop_begin,
+                            int32_t loop_count, const int32_t* ctx_lens, int32_t max_ctx,
+                            uint16_t* out) {
   if (!q || !ctx_lens || !out) return RQ_ERR_INVALID_ARG;
   if (loop_count < 1 || loop_begin < 0 || loop_begin + loop_count > s->n_loops)
     return RQ_ERR_INVALID_ARG;
   if (max_ctx < 0 || max_ctx > s->capacity) return RQ_ERR_INVALID_ARG;
   if (int64_t(s->batch) * s->n_q_heads * loop_count > (int64_t(1) << 31))
     return RQ_ERR_UNSUPPORTED;
+  return RQ_OK;
+}
+
+rq_status check_decode(const rq_shape* s, const uint16_t* q, int32_t loop_begin,
+                       int32_t loop_count, const int32_t* ctx_lens, int32_t max_ctx,
+                       uint16_t* out, void* ws, size_t ws_bytes) {
+  const rq_status st = check_decode_args(s, q, loop_begin, loop_count, ctx_lens, max_ctx, out);
+  if (st != RQ_OK) return st;
   const size_t need = rq_decode_workspace_bytes(s, loop_count, max_ctx);
   if (!ws || ws_bytes < need) return RQ_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return RQ_ERR_WORKSPACE;
@@ -102,7 +112,8 @@ rq_status encode_common(const rq_shape* shape, const rq_cache* cache, const rq_p
 rq_status decode_common(const rq_shape* shape, const rq_cache* cache, const rq_paging* paging,
                         const uint16_t* q, int32_t loop_begin, int32_t loop_count,
                         const uint16_t* pending_kv, const int32_t* ctx_lens, int32_t max_ctx,
-                        uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+                        uint16_t* out, void* ws, size_t ws_bytes, void* stream,
+                        const rq::DecodeHooks* hooks = nullptr) {
   rq_status st = check_shape(shape);
   if (st != RQ_OK) return st;
   if ((st = check_cache(shape, cache)) != RQ_OK) return st;
@@ -114,13 +125,28 @@ rq_status decode_common(const rq_shape* shape, const rq_cache* cache, const rq_p
     return from_cuda(rq::launch_rq_decode(*shape, *cache, paging, q, loop_begin, loop_count,
                                           pending_kv, ctx_lens, max_ctx, out,
                                           static_cast<float*>(ws),
-                                          static_cast<cudaStream_t>(stream)));
+                                          static_cast<cudaStream_t>(stream), hooks));
   } catch (...) {
     return RQ_ERR_INTERNAL;
   }
 }
 
 }  // namespace
+
+namespace rq {
+
+// Every check rq_decode_attention makes before its workspace check, in the same order, so
+// that an entry point with its own scratch returns the same status for the same arguments.
+rq_status validate_decode(const rq_shape* shape, const rq_cache* cache, const uint16_t* q,
+                          int32_t loop_begin, int32_t loop_count, const int32_t* ctx_lens,
+                          int32_t max_ctx, uint16_t* out) {
+  rq_status st = check_shape(shape);
+  if (st != RQ_OK) return st;
+  if ((st = check_cache(shape, cache)) != RQ_OK) return st;
+  return check_decode_args(shape, q, loop_begin, loop_count, ctx_lens, max_ctx, out);
+}
+
+}  // namespace rq
 
 extern "C" {
 
@@ -196,6 +222,18 @@ rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k, con
   } catch (...) {
     return RQ_ERR_INTERNAL;
   }
+}
+
+rq_status rq_test_decode_attention_wait_runs_out(const rq_shape* shape, const rq_cache* cache,
+                                                 const uint16_t* q, int32_t loop_begin,
+                                                 int32_t loop_count, const uint16_t* pending_kv,
+                                                 const int32_t* ctx_lens, int32_t max_ctx,
+                                                 uint16_t* out, void* ws, size_t ws_bytes,
+                                                 uint64_t wait_limit_ns, void* stream) {
+  if (wait_limit_ns == 0 || wait_limit_ns > 2000000000ull) return RQ_ERR_INVALID_ARG;
+  const rq::DecodeHooks hooks{wait_limit_ns, true};
+  return decode_common(shape, cache, nullptr, q, loop_begin, loop_count, pending_kv, ctx_lens,
+                       max_ctx, out, ws, ws_bytes, stream, &hooks);
 }
 
 rq_status rq_advance_ctx(int32_t* ctx_lens, int32_t batch, int32_t n, int32_t capacity,

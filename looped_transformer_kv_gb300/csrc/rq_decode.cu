@@ -94,7 +94,7 @@ cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const rq_
                              const uint16_t* q,
                              int loop_begin, int loop_count, const uint16_t* pending,
                              const int32_t* ctx_lens, int max_ctx, uint16_t* out, float* ws,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const DecodeHooks* hooks) {
   const SplitPlan plan = plan_splits_rq(s, loop_begin, loop_count, max_ctx);
   unsigned* err = reinterpret_cast<unsigned*>(ws);
   const size_t tb = ws_ticket_bytes(s, loop_count);
@@ -105,7 +105,7 @@ cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const rq_
   const bool in_kernel = decode_combines_in_kernel(s, loop_begin, loop_count);
   e = launch_rq_decode_mma(s, cache, paging, q, loop_begin, loop_count, ctx_lens, plan.n_splits,
                            plan.tokens_per_split, pending, out, part, in_kernel ? tickets : nullptr,
-                           err, stream);
+                           err, stream, hooks);
   if (e != cudaSuccess) return e;
   if (in_kernel) return cudaSuccess;
   return launch_combine(s, cache.rot_signs[1], q, loop_count, pending, plan.n_splits, out, part,

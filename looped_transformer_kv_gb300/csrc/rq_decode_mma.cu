@@ -195,7 +195,8 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
                                  const uint16_t* q, int loop_begin, int loop_count,
                                  const int32_t* ctx_lens, int n_splits, int tokens_per_split,
                                  const uint16_t* pending, uint16_t* out, float* part,
-                                 unsigned* tickets, unsigned* err, cudaStream_t stream) {
+                                 unsigned* tickets, unsigned* err, cudaStream_t stream,
+                                 const DecodeHooks* hooks) {
   cudaError_t e = prepare_kernels();
   if (e != cudaSuccess) return e;
   QueryBlock blocks[64];
@@ -231,6 +232,8 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
     a.n_splits = n_splits;
     a.tokens_per_split = tokens_per_split;
     a.scale_log2 = scale * kLog2e;
+    a.wait_limit_ns = hooks ? hooks->wait_limit_ns : kWaitLimitNs;
+    a.withhold_first_tile = hooks && hooks->withhold_first_tile ? 1 : 0;
     dim3 grid(n_splits, s.n_kv_heads, s.batch);
     pick(s.head_dim, bl.res4, blocks[bi].nr, paging != nullptr, block_packing(blocks[bi]))<<<grid, kW * 32, bl.smem, stream>>>(a);
     e = cudaGetLastError();

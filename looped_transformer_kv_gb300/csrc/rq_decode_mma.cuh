@@ -77,6 +77,8 @@ struct MmaArgs {
   float scale_log2;
   int n_stages, stage_bytes;
   int qrm_bytes;             // masked rotated-query fragments (masked_fragment_bytes)
+  uint64_t wait_limit_ns;     // pipeline wait limit (kWaitLimitNs in product calls)
+  int withhold_first_tile;    // test hook: tile 0 of every split is never copied
   const int32_t* bt;   // block table of a paged cache, or null
   int max_pages, n_pages, n_pg;   // table columns, physical pages, page-id slots in shared memory
   int off_kc, off_km, off_vc, off_vm;
@@ -321,8 +323,14 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
 
   // ------------------------------------------------------------------ pipeline set-up
   // (first: the first tiles stream in while the queries are prepared)
-  const int ctx = min(a.ctx_lens[b], a.cap);
+  const int ctx_raw = a.ctx_lens[b];
+  const int ctx = min(ctx_raw, a.cap);
   const int t_begin = split * a.tokens_per_split;
+  // a context longer than the call's splits cover (ctx_len above max_ctx or the capacity) or
+  // negative is refused: the call is flagged (outputs NaN) rather than silently truncated
+  if (split == a.n_splits - 1 && threadIdx.x == 0 &&
+      (ctx_raw < 0 || ctx_raw > a.cap || int64_t(ctx_raw) > int64_t(a.n_splits) * a.tokens_per_split))
+    atomicOr(a.err, 1u);
   const int t_end = min(ctx, t_begin + a.tokens_per_split);
   const int ntiles = t_end > t_begin ? (t_end - t_begin + kT - 1) / kT : 0;
   const int64_t slot = int64_t(b) * a.H + h;
@@ -347,6 +355,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   }
 
   auto issue = [&](int tile) {
+    if (a.withhold_first_tile && tile == 0) return;   // (test hook: the wait can only run out)
     const int st = tile % S;
     const uint32_t bar = smem_u32(&bars[st]);
     const uint32_t dst = smem_u32(smem + st * a.stage_bytes);
@@ -591,7 +600,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % S;
     if (!__all_sync(RQ_FULL_MASK,
-                    mbar_wait_bounded(smem_u32(&bars[st]), uint32_t((i / S) & 1), kWaitLimitNs))) {
+                    mbar_wait_bounded(smem_u32(&bars[st]), uint32_t((i / S) & 1), a.wait_limit_ns))) {
       failed = true;
       break;
     }
@@ -1150,7 +1159,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
       atomicOr(a.err, 1u);
       const int issued = int(cnt[kIssuedSlot]);
       for (int t = issued - S < 0 ? 0 : issued - S; t < issued; ++t)
-        mbar_wait_bounded(smem_u32(&bars[t % S]), uint32_t((t / S) & 1), kWaitLimitNs);
+        mbar_wait_bounded(smem_u32(&bars[t % S]), uint32_t((t / S) & 1), a.wait_limit_ns);
     }
     combine_if_last();
     return;

@@ -72,6 +72,14 @@ __host__ __device__ inline SmemLayout smem_layout(int D, bool res4, int stages, 
 // Split partial record: m, l, two pad floats, acc_ref[D], acc_res[D] (16-byte aligned rows).
 __host__ __device__ constexpr size_t partial_floats_d(int D) { return size_t(4 + 2 * D); }
 
+// Test hooks of a decode call (null in every product call): the pipeline wait limit, and
+// whether the copy of each split's first tile is withheld, so that the wait for it can only
+// run out (nothing is in flight for it) and the bounded-wait failure path runs.
+struct DecodeHooks {
+  uint64_t wait_limit_ns;
+  bool withhold_first_tile;
+};
+
 int plan_query_blocks(const rq_shape& s, int loop_begin, int loop_count, QueryBlock* out,
                       int max_out);
 
@@ -84,7 +92,8 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
                                  const uint16_t* q, int loop_begin, int loop_count,
                                  const int32_t* ctx_lens, int n_splits, int tokens_per_split,
                                  const uint16_t* pending, uint16_t* out, float* part,
-                                 unsigned* tickets, unsigned* err, cudaStream_t stream);
+                                 unsigned* tickets, unsigned* err, cudaStream_t stream,
+                                 const DecodeHooks* hooks = nullptr);
 
 struct SplitPlan {
   int n_splits;          // split-KV partitions of the context
@@ -108,7 +117,7 @@ cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const rq_
                              const uint16_t* q,
                              int loop_begin, int loop_count, const uint16_t* pending,
                              const int32_t* ctx_lens, int max_ctx, uint16_t* out, float* ws,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const DecodeHooks* hooks = nullptr);
 
 cudaError_t launch_bf16_decode(const rq_shape& s, const uint16_t* k, const uint16_t* v,
                                const uint16_t* q, int loop_begin, int loop_count,
@@ -121,5 +130,10 @@ cudaError_t launch_combine(const rq_shape& s, const int8_t* v_signs, const uint1
                            cudaStream_t stream);
 
 int device_sm_count();
+
+// The argument checks of rq_decode_attention other than its workspace (C ABI layer).
+rq_status validate_decode(const rq_shape* shape, const rq_cache* cache, const uint16_t* q,
+                          int32_t loop_begin, int32_t loop_count, const int32_t* ctx_lens,
+                          int32_t max_ctx, uint16_t* out);
 
 }  // namespace rq

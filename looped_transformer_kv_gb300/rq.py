@@ -164,6 +164,16 @@ def decode_attention_noalloc(shape, cache, q, loop_begin, loop_count, pending_kv
         _stream(stream)))
 
 
+def test_decode_attention_wait_runs_out(shape, cache, q, loop_begin, loop_count, pending_kv,
+                                        ctx_lens, max_ctx, out, ws, wait_limit_ns, stream=None):
+    """rq_test_decode_attention_wait_runs_out (test hook, include/rq_test.h)."""
+    check("rq_test_decode_attention_wait_runs_out",
+          _lib.lib().rq_test_decode_attention_wait_runs_out(
+              ctypes.byref(shape), ctypes.byref(cache.struct), _ptr(q), int(loop_begin),
+              int(loop_count), _ptr(pending_kv), _ptr(ctx_lens), int(max_ctx), _ptr(out), _ptr(ws),
+              ws.numel() * ws.element_size(), int(wait_limit_ns), _stream(stream)))
+
+
 def noalloc_scratch_bytes():
     return int(_lib.lib().rq_decode_noalloc_scratch_bytes())
 
