@@ -6,11 +6,18 @@ decode attention of every loop over the packed cache (all loops' queries in one 
 reference tile read once) plus the deferred write of the current token (encode + append of
 its L loop states).  Metric: KV tokens/s = batch * ctx * loops * layers / step time.
 
+The headline workload is the serving-scale one (B 128, ctx 32768, 16 heads, d 128, 4 loops,
+decode and deferred-write encode interleaved in a step).  The line's `breakdown` also carries,
+measured in the same run, every other workload (per-layer times, all 24 layers for mixed_24l),
+the BF16 comparison kernel on the same shapes, the paged cache, the serving step under a CUDA
+graph, the bulk prefill encode and the fixed KV-memory budget experiment.
+
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                [--no-sweep] [--no-bf16] [--no-paged] [--no-cpu-baseline] [--budget-gb G]
 
 With --gpus N > 1 (launched by torch.distributed.run) every rank runs the whole workload on
 its own GPU (independent sequences: weak scaling, no collective on the data path); times
-are max-reduced over ranks.  --impl reference times the fp64 CPU oracle on host cores.
+are max-reduced over ranks.  --impl reference times the fp64 CPU oracle on the host cores.
 """
 
 import argparse
@@ -28,16 +35,14 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn KV tokens/s at 1 GB300, HBM GB/s vs peak, vs in-build BF16 kernel"
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one all-loops decode launch
-# of the split kernel, from one ncu capture (profiles/), keyed by the kernel sources they
-# were taken on; any change to those sources makes the figure stale (reported as null).
+# of the split kernel, from one ncu capture, keyed by the kernel sources they were taken on;
+# any change to those sources makes the figure stale (reported as null).
 KERNEL_SOURCES = ("looped_transformer_kv_gb300/csrc/rq_decode_mma.cu",
                   "looped_transformer_kv_gb300/csrc/rq_decode_mma.cuh",
                   "looped_transformer_kv_gb300/csrc/rq_ptx.cuh",
                   "looped_transformer_kv_gb300/csrc/rq_common.cuh",
                   "looped_transformer_kv_gb300/csrc/rq_kernels.h")
-TRAFFIC = {
-    ("7a5789489900c373", "layer_1p4b"): 483010304 + 11158272,  # profiles/rq_mma_kernel_layer_1p4b.md
-}
+TRAFFIC = {}
 
 
 def _kernel_hash():
@@ -50,8 +55,7 @@ def _kernel_hash():
 
 
 def _traffic(workload):
-    t = TRAFFIC.get((_kernel_hash(), workload))
-    return t
+    return TRAFFIC.get((_kernel_hash(), workload))
 
 
 def reduce_step_ms(ms, world):
@@ -75,67 +79,118 @@ def _peaks():
 
 
 # ---------------------------------------------------------------------------- oracle arm
+#
+# The fp64 oracle's decode (rotated form) of all loops, timed on its own: slices of the
+# workload (one sequence and kv-head each) are generated and encoded first (untimed), then
+# every worker process -- one per host core, one BLAS thread each -- decodes its slices in
+# rounds that start together; a round's wall clock is taken between two barriers.
 
-ORACLE_SNIPPET = r"""
-import json, sys, time
-import numpy as np
-sys.path.insert(0, %(root)r)
-import oracle as O, synth
-cfg = synth.config_by_name(%(name)r)
-heads = %(heads)r
-slices = []
-for h in heads:
-    x = synth.gen_states(cfg, 0, [0], np.arange(cfg.ctx + 1), heads=[h])[0, :, :, :, 0, :].astype(np.float64)
-    s = synth.rotation_signs(cfg, 0)[h].astype(np.float64)
+_BLAS_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def _oracle_worker(name, slices, rounds, barrier, results):
+    import numpy as np
+
+    import oracle as O
+    import synth
+    cfg = synth.config_by_name(name)
     rb = cfg.res_bits[: cfg.n_loops - 1]
-    ek = O.encode(x[:cfg.ctx, 0], s[0], rb)
-    ev = O.encode(x[:cfg.ctx, 1], s[1], rb)
-    q = synth.gen_queries(cfg, 0, [0])[0].astype(np.float64)
     g = cfg.n_q_heads // cfg.n_kv_heads
-    slices.append((ek, ev, s, q[h * g:(h + 1) * g], x[cfg.ctx]))
-def one_pass():
-    for ek, ev, s, q, pend in slices:
-        for l in range(cfg.n_loops):
-            O.decode_rotated(q[:, l], ek, ev, s[0], s[1], l, pend[0, l], pend[1, l])
-tok = len(slices) * cfg.ctx * cfg.n_loops
-times = []
-for i in range(%(warmup)d):
-    one_pass()
-t_all = time.perf_counter()
-reps = 0
-while True:
-    t0 = time.perf_counter(); one_pass(); times.append(time.perf_counter() - t0); reps += 1
-    if reps >= %(min_reps)d and time.perf_counter() - t_all >= %(min_s)f:
-        break
-print(json.dumps({"times": times, "tokens_per_pass": tok}))
-"""
+    signs = synth.rotation_signs(cfg, 0)
+    prepared = []
+    for b, h in slices:
+        x = synth.gen_states(cfg, 0, [b], np.arange(cfg.ctx + 1), heads=[h])[0, :, :, :, 0, :]
+        x = x.astype(np.float64)
+        s = signs[h].astype(np.float64)
+        ek = O.encode(x[:cfg.ctx, 0], s[0], rb)
+        ev = O.encode(x[:cfg.ctx, 1], s[1], rb)
+        q = synth.gen_queries(cfg, 0, [b])[0, h * g:(h + 1) * g].astype(np.float64)
+        prepared.append((ek, ev, s, q, x[cfg.ctx]))
+    barrier.wait()                                  # every worker's slices are ready
+    for _ in range(rounds):
+        barrier.wait()                              # round start
+        for ek, ev, s, q, pend in prepared:
+            for l in range(cfg.n_loops):
+                O.decode_rotated(q[:, l], ek, ev, s[0], s[1], l, pend[0, l], pend[1, l])
+        barrier.wait()                              # round end
+    results.put(len(prepared))
 
 
-def run_oracle(name, heads, warmup, min_reps, min_s):
-    env = dict(os.environ)
-    n = os.cpu_count() or 1
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[k] = str(n)
-    code = ORACLE_SNIPPET % dict(root=ROOT, name=name, heads=list(heads), warmup=warmup,
-                                 min_reps=min_reps, min_s=min_s)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
-    if r.returncode != 0:
-        raise RuntimeError("oracle run failed: " + r.stderr[-2000:])
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    return d["times"], d["tokens_per_pass"], n
+def run_oracle(name, n_workers, per_worker, rounds):
+    """Round wall-clock times (s) of the oracle decode on n_workers processes, each with
+    per_worker slices spread over the batch and heads; returns (times, kv_tokens_per_round,
+    description of the sample)."""
+    import multiprocessing as mp
+
+    import synth
+    cfg = synth.config_by_name(name)
+    units = [(b, h) for b in range(cfg.batch) for h in range(cfg.n_kv_heads)]
+    n = min(len(units), n_workers * per_worker)
+    stride = len(units) / n
+    chosen = [units[int(i * stride)] for i in range(n)]
+    work = [chosen[i::n_workers] for i in range(n_workers)]
+    work = [w for w in work if w]
+    saved = {k: os.environ.get(k) for k in _BLAS_ENV}
+    for k in _BLAS_ENV:
+        os.environ[k] = "1"
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(len(work) + 1)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(name, w, rounds, barrier, results))
+             for w in work]
+    try:
+        for p in procs:
+            p.start()
+        barrier.wait(timeout=1800)                  # slices generated and encoded
+        times = []
+        for _ in range(rounds):
+            barrier.wait(timeout=1800)
+            t0 = time.perf_counter()
+            barrier.wait(timeout=1800)
+            times.append(time.perf_counter() - t0)
+        done = sum(results.get(timeout=600) for _ in procs)
+        for p in procs:
+            p.join(timeout=600)
+    finally:
+        for p in procs:
+            if p.is_alive():
+                p.terminate()
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    assert done == n
+    tokens = n * cfg.ctx * cfg.n_loops
+    desc = ("%d of the %d (sequence, kv-head) slices, spread over the batch, each: fp64 oracle "
+            "decode (rotated form) of all %d loops over ctx %d; %d worker process(es), one "
+            "BLAS thread each" % (n, len(units), cfg.n_loops, cfg.ctx, len(work)))
+    return times, tokens, desc
+
+
+def cpu_baseline(name, rounds=3):
+    """All host cores over a fraction of the slices, and one core on one slice."""
+    cores = os.cpu_count() or 1
+    t1, tok1, _ = run_oracle(name, 1, 1, rounds)
+    single = tok1 / statistics.median(t1)
+    tn, tokn, desc = run_oracle(name, cores, 1, rounds)
+    value = tokn / statistics.median(tn)
+    return {"value": value, "unit": "KV tokens/s", "cores": cores, "kind": "oracle",
+            "sample": desc + "; median of %d rounds" % rounds,
+            "single_thread": {"value": single, "unit": "KV tokens/s",
+                              "sample": "one slice, one process, one BLAS thread"}}
 
 
 def reference_arm(args, cfg):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    heads = [0]
-    times, tok, cores = run_oracle(cfg.name, heads, args.warmup, args.steps, 0.0)
-    times = times[: args.steps]
+    cores = os.cpu_count() or 1
+    times, tok, desc = run_oracle(cfg.name, cores, 1, args.warmup + args.steps)
+    times = times[args.warmup:]
     t = sum(times)
     value = tok * len(times) / t
-    sample = ("sequence 0, kv-head 0: fp64 oracle decode (rotated form) of all %d loops over "
-              "ctx %d per step" % (cfg.n_loops, cfg.ctx))
+    sample = desc + "; a step is one round over the sampled slices"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "KV tokens/s",
             "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
             "ms_per_step": 1e3 * t / len(times), "higher_is_better": True,
@@ -201,6 +256,176 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
+def graph_of(fn):
+    """Capture fn (a sequence of library calls on the current stream) in a CUDA graph."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        fn()
+    torch.cuda.synchronize()
+    return gr
+
+
+def timeit(gr, iters, warmup=3):
+    """Per-replay device times (ms) of a captured graph, CUDA events on the current stream."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        gr.replay()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(iters):
+        gr.replay()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
+
+
+def byte_counts(cfg, w, out):
+    """Algorithmic bytes of one layer's decode call: all-loops, per-loop (sum of the L calls)
+    and the BF16 kernel, each with the queries, current token and outputs."""
+    L, d = cfg.n_loops, cfg.head_dim
+    ng = d // 32
+    ref_b = 2 * (d // 2 + 4 * ng)
+    res_b = [2 * (d * b // 8 + 4 * ng + 2) for b in cfg.res_bits[: L - 1]]
+    th = w.B * w.H * cfg.ctx
+    io_b = w.q.numel() * 2 + w.pending.numel() * 2 + out.numel() * 2
+    return {"multi": th * (ref_b + sum(res_b)) + io_b,
+            "per": th * (L * ref_b + sum(res_b)) + io_b,
+            "bf16": th * L * 2 * d * 2 + io_b,
+            "per_token_head_multi": ref_b + sum(res_b), "ref_b": ref_b, "res_b": res_b}
+
+
+def _row(ms, kvtok, nbytes, hbm):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": ms, "kv_tokens_s": kvtok / (ms * 1e-3), "gbs": gbs, "frac_hbm_measured": gbs / hbm,
+            "frac_hbm_nominal_8tbs": gbs / 8000.0}
+
+
+def decode_timings(w, iters, bf16, L):
+    """Graph-replayed per-call times (ms, medians) of workload w's all-loops and per-loop
+    decode calls, and of the BF16 kernel's on the same shapes if built."""
+    med = statistics.median
+    out, ws, ws1 = w.out_buffer(L), w.workspace(L), w.workspace(1)
+    out1 = [w.out_buffer(1) for _ in range(L)]
+    t = {"multi": med(timeit(graph_of(lambda: w.decode(0, L, out, ws)), iters))}
+
+    def per():
+        for l in range(L):
+            w.decode(l, 1, out1[l], ws1)
+
+    t["per"] = med(timeit(graph_of(per), iters))
+    if bf16:
+        t["bf16_multi"] = med(timeit(graph_of(lambda: w.decode_bf16(0, L, out, ws)), iters))
+
+        def bf_per():
+            for l in range(L):
+                w.decode_bf16(l, 1, out1[l], ws1)
+
+        t["bf16_per"] = med(timeit(graph_of(bf_per), iters))
+    return t, out
+
+
+def workload_rows(cfg, nb, t, hbm, layers=1):
+    """Breakdown rows of one workload from its per-layer times (t: decode_timings) and byte
+    counts (nb: byte_counts)."""
+    L = cfg.n_loops
+    kvtok = cfg.batch * cfg.ctx * L
+    rows = {"rq_decode_multiloop": _row(t["multi"], kvtok, nb["multi"], hbm),
+            "rq_decode_perloop": _row(t["per"], kvtok, nb["per"], hbm)}
+    if "bf16_multi" in t:
+        rows["bf16_decode_multiloop"] = _row(t["bf16_multi"], kvtok, nb["bf16"], hbm)
+        rows["bf16_decode_perloop"] = _row(t["bf16_per"], kvtok, nb["bf16"], hbm)
+        rows["speedup_vs_bf16"] = {"multiloop": t["bf16_multi"] / t["multi"],
+                                   "perloop": t["bf16_per"] / t["per"]}
+    if layers > 1:
+        rows["layers"] = layers
+        rows["note"] = ("times are per layer (mean over all %d layers, each timed on its own "
+                        "cache); BF16 timed on layer 0" % layers)
+    return rows
+
+
+def sweep_workload(name, iters, hbm):
+    """Another workload at full size: all-loops and per-loop decode per layer, the BF16
+    kernel on the same shapes; multi-layer workloads time every layer in turn (each layer's
+    cache built, timed and freed)."""
+    import torch
+
+    import synth
+    from looped_transformer_kv_gb300.workload import Workload
+    cfg = synth.config_by_name(name)
+    L = cfg.n_loops
+    tm, tp = [], []
+    t0 = nb = None
+    for layer in range(cfg.layers):
+        w = Workload(cfg, layer=layer, capacity=cfg.ctx + 2, build_bf16=(layer == 0))
+        t, out = decode_timings(w, iters, layer == 0, L)
+        tm.append(t["multi"])
+        tp.append(t["per"])
+        if layer == 0:
+            t0, nb = t, byte_counts(cfg, w, out)
+        del w, out
+        torch.cuda.empty_cache()
+    t = dict(t0)
+    t["multi"] = statistics.mean(tm)
+    t["per"] = statistics.mean(tp)
+    rows = workload_rows(cfg, nb, t, hbm, cfg.layers)
+    rows["workload"] = _workload_desc(cfg)
+    if cfg.layers > 1:
+        rows["model_step_ms"] = {"multiloop": sum(tm), "perloop": sum(tp)}
+        rows["layer_ms_range"] = {"multiloop": [min(tm), max(tm)], "perloop": [min(tp), max(tp)]}
+    return rows
+
+
+def budget_experiment(name, budget_gib, iters):
+    """Fixed KV-memory budget per layer: the largest batch whose cache fits, for the packed and
+    for the BF16 cache, and decode KV tokens/s of each at its own batch."""
+    import torch
+
+    import synth
+    from looped_transformer_kv_gb300.workload import Workload, budget_batches
+    cfg = synth.config_by_name(name)
+    budget = int(budget_gib * (1 << 30))
+    cap = max(64, -(-(cfg.ctx + 2) // 64) * 64)
+    L = cfg.n_loops
+    b_rq, b_bf, rq_seq, bf_seq = budget_batches(cfg, budget, cap)
+    res = {"experiment": "fixed KV-memory budget per layer", "workload": _workload_desc(cfg),
+           "budget_gib": budget_gib, "bytes_per_sequence": {"rq": rq_seq, "bf16": bf_seq}}
+    med = statistics.median
+    for kind, B in (("rq", b_rq), ("bf16", b_bf)):
+        w = Workload(cfg, capacity=cap, batch=int(B), build_rq=kind == "rq",
+                     build_bf16=kind == "bf16")
+        out, ws = w.out_buffer(L), w.workspace(L)
+        out1, ws1 = [w.out_buffer(1) for _ in range(L)], w.workspace(1)
+        dec = w.decode if kind == "rq" else w.decode_bf16
+        t_multi = med(timeit(graph_of(lambda: dec(0, L, out, ws)), iters))
+
+        def per():
+            for l in range(L):
+                dec(l, 1, out1[l], ws1)
+
+        t_per = med(timeit(graph_of(per), iters))
+        kvtok = B * cfg.ctx * L
+        res[kind] = {"batch": int(B), "cache_gib": B * (rq_seq if kind == "rq" else bf_seq) / 2**30,
+                     "multiloop_ms": t_multi, "multiloop_kv_tokens_s": kvtok / (t_multi * 1e-3),
+                     "perloop_ms": t_per, "perloop_kv_tokens_s": kvtok / (t_per * 1e-3)}
+        del w, out, ws, out1, ws1
+        torch.cuda.empty_cache()
+    res["batch_ratio"] = res["rq"]["batch"] / res["bf16"]["batch"]
+    res["throughput_ratio_multiloop"] = (res["rq"]["multiloop_kv_tokens_s"] /
+                                         res["bf16"]["multiloop_kv_tokens_s"])
+    res["throughput_ratio_perloop"] = (res["rq"]["perloop_kv_tokens_s"] /
+                                       res["bf16"]["perloop_kv_tokens_s"])
+    return res
+
+
 def gpu_arm(args, cfg):
     import torch
     import torch.distributed as dist
@@ -211,21 +436,15 @@ def gpu_arm(args, cfg):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle runs in spawned processes before this one touches the GPU
+        cpu = cpu_baseline(cfg.name)
+
     if world > 1:
         dist.init_process_group("gloo")
     torch.cuda.set_device(local)
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        # the oracle runs in a fresh process before this one touches the GPU
-        times, tok, cores = run_oracle(cfg.name, list(range(min(4, cfg.n_kv_heads))), 1, 1,
-                                       args.cpu_seconds)
-        cpu = {"value": tok * len(times) / sum(times), "unit": "KV tokens/s", "cores": cores,
-               "kind": "oracle",
-               "sample": "sequence 0, kv-heads 0..%d (ctx %d, all %d loops), fp64 oracle decode "
-                         "(rotated form) repeated %d times, %.1f s" %
-                         (min(4, cfg.n_kv_heads) - 1, cfg.ctx, cfg.n_loops, len(times),
-                          sum(times))}
 
     # spare slots past ctx: the deferred write of the current token lands in slot ctx,
     # which the step's attention (ctx_lens = ctx) does not read, so every step is the same.
@@ -236,16 +455,10 @@ def gpu_arm(args, cfg):
     w = layers[0]
     NL = len(layers)
     L, B, ctx = cfg.n_loops, w.B, cfg.ctx
-    stream = torch.cuda.current_stream()
-    out = w.out_buffer(L)
     ws = w.workspace(L)
-    ws1 = w.workspace(1)
-    out1 = [w.out_buffer(1) for _ in range(L)]
+    outs = [lw.out_buffer(L) for lw in layers]
     # deferred write of the current token: its L states, appended at slot ctx
-    new_kv = w.pending.reshape(B, 1, 2, L, w.H, w.d)
     pos_new = torch.full((B, 1), ctx, dtype=torch.int32, device="cuda")
-
-    outs = [out] + [lw.out_buffer(L) for lw in layers[1:]]
 
     def step():
         for lw, o in zip(layers, outs):
@@ -259,31 +472,6 @@ def gpu_arm(args, cfg):
     combine = 0 if (g * L == 1 and w.d == 128) else 1
     launches_per_step = NL * (math.ceil(g * L / 8) + combine + 1)
 
-    def graph_of(fn):
-        """Capture fn (a sequence of library calls on the current stream) in a CUDA graph."""
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            fn()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr):
-            fn()
-        torch.cuda.synchronize()
-        return gr
-
-    def timeit(gr, iters):
-        """Per-replay device times (ms) of a captured graph, CUDA events on this stream."""
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
-        torch.cuda.synchronize()
-        ev[0].record(stream)
-        for i in range(iters):
-            gr.replay()
-            ev[i + 1].record(stream)
-        torch.cuda.synchronize()
-        return [ev[i].elapsed_time(ev[i + 1]) for i in range(iters)]
-
     g_step = graph_of(step)
     # ---- warm-up, then the timed steps (barrier + synchronize on both sides) ----
     for _ in range(args.warmup):
@@ -293,6 +481,7 @@ def gpu_arm(args, cfg):
         dist.barrier()
     clocks = Clocks(local)
     time.sleep(0.3)
+    stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -305,37 +494,36 @@ def gpu_arm(args, cfg):
     if world > 1:
         dist.barrier()
 
-    # ---- per-call timings (graph replays, same stream, CUDA events) ----
+    # ---- per-call timings of the headline workload (graph replays, CUDA events) ----
     iters = max(args.steps, 20)
-    t_dec = timeit(graph_of(lambda: w.decode(0, L, out, ws)), iters)
+    med = statistics.median
+    hbm, peak_kind = _peaks()
+    t, out = decode_timings(w, iters, not args.no_bf16, L)
+    new_kv = w.pending.reshape(B, 1, 2, L, w.H, w.d)
     t_enc = timeit(graph_of(lambda: rqm.encode_append(w.shape, w.cache, new_kv, positions=pos_new)),
                    iters)
-
-    def perloop():
-        for l in range(L):
-            w.decode(l, 1, out1[l], ws1)
-
-    t_per = timeit(graph_of(perloop), iters)
-    t_bf_multi = t_bf_per = None
-    if not args.no_bf16:
-        t_bf_multi = timeit(graph_of(lambda: w.decode_bf16(0, L, out, ws)), iters)
-
-        def bf_per():
-            for l in range(L):
-                w.decode_bf16(l, 1, out1[l], ws1)
-
-        t_bf_per = timeit(graph_of(bf_per), iters)
+    nb = byte_counts(cfg, w, out)
+    breakdown = workload_rows(cfg, nb, t, hbm)
+    breakdown["encode_append_us"] = 1e3 * med(t_enc)
+    breakdown["interleaved_step_ms"] = ms / NL
+    breakdown["storage_reduction_vs_bf16"] = 1 - nb["per_token_head_multi"] / (L * 2 * cfg.head_dim * 2)
+    out1 = [w.out_buffer(1) for _ in range(L)]
+    ws1 = w.workspace(1)
     # the same tokens in a paged cache (64-token pages scattered over a pool with spare pages)
-    t_pg_multi = t_pg_per = None
     if not args.no_paged:
         pc, paging, bt = w.paged_twin(spare_pages=64, seed=1)
-        t_pg_multi = timeit(graph_of(lambda: w.decode_paged(pc, paging, 0, L, out, ws)), iters)
+        t_pg_multi = med(timeit(graph_of(lambda: w.decode_paged(pc, paging, 0, L, out, ws)), iters))
 
         def pg_per():
             for l in range(L):
                 w.decode_paged(pc, paging, l, 1, out1[l], ws1)
 
-        t_pg_per = timeit(graph_of(pg_per), iters)
+        t_pg_per = med(timeit(graph_of(pg_per), iters))
+        kvtok = B * ctx * L
+        for name, tt, nbytes, base in (("rq_paged_decode_multiloop", t_pg_multi, nb["multi"], t["multi"]),
+                                       ("rq_paged_decode_perloop", t_pg_per, nb["per"], t["per"])):
+            breakdown[name] = _row(tt, kvtok, nbytes, hbm)
+            breakdown[name]["time_vs_contiguous"] = tt / base
         del pc, paging, bt
         torch.cuda.empty_cache()
     # serving step: the L per-loop decode calls, the deferred write of the token into slot
@@ -343,15 +531,27 @@ def gpu_arm(args, cfg):
     # spare capacity past ctx takes the appended tokens)
     ctx_srv = w.ctx_lens.clone()
     ws_srv = w.workspace_for(1, w.cap)
-    t_srv = timeit(graph_of(lambda: w.serving_step(ctx_srv, out1, ws_srv, w.cap)), iters)
+    t_srv = timeit(graph_of(lambda: w.serving_step(ctx_srv, out1, ws_srv, w.cap)), iters, warmup=0)
     grown = int((ctx_srv - w.ctx_lens).max().item())
+    m = med(t_srv)
+    breakdown["serving_step"] = {
+        "what": "per-loop decode of all %d loops + encode of the token + ctx advance, one CUDA "
+                "graph replayed %d times (ctx %d..%d)" % (L, len(t_srv), ctx, ctx + grown),
+        "ms": m, "tokens_s": B / (m * 1e-3), "kv_tokens_s": B * ctx * L / (m * 1e-3)}
     # bulk prefill encode: n_pre tokens of every sequence in one call (their own states, so
     # the cache is rewritten with the same bytes)
     n_pre = min(2048, ctx)
-    pre = torch.empty(B, n_pre, 2, L, w.H, w.d, dtype=torch.bfloat16, device="cuda")
-    rqm.synth_states(w.params, pre, pre.stride()[:5], 0, B, 0, n_pre, 0, L)
-    t_pre = timeit(graph_of(lambda: rqm.encode_append(w.shape, w.cache, pre, pos_begin=0)), iters)
-    pre_bytes = pre.numel() * 2
+    bpre = min(B, 16)
+    pre = torch.empty(bpre, n_pre, 2, L, w.H, w.d, dtype=torch.bfloat16, device="cuda")
+    rqm.synth_states(w.params, pre, pre.stride()[:5], 0, bpre, 0, n_pre, 0, L)
+    sub = w._sub_cache(0, bpre)
+    sub_shape = rqm.make_shape(bpre, w.Hq, w.H, w.d, L, w.cap, cfg.res_bits[: L - 1])
+    t_pre = timeit(graph_of(lambda: rqm.encode_append(sub_shape, sub, pre, pos_begin=0)), iters)
+    m = med(t_pre)
+    breakdown["prefill_encode"] = {
+        "what": "rq_encode_append of %d tokens x %d sequences in one call" % (n_pre, bpre),
+        "ms": m, "tokens_s": bpre * n_pre / (m * 1e-3),
+        "gbs": (pre.numel() * 2 + bpre * n_pre * w.H * nb["per_token_head_multi"]) / (m * 1e-3) / 1e9}
     del pre
     torch.cuda.empty_cache()
     clk = clocks.stop()
@@ -384,61 +584,24 @@ def gpu_arm(args, cfg):
     h2d = sum(x.numel() * 2 for x in q_h + p_h)
     d2h = sum(x.numel() * 2 for x in o_h)
 
-    # ---- bytes ----
-    d, ng = cfg.head_dim, cfg.head_dim // 32
-    ref_b = 2 * (d // 2 + 4 * ng)
-    res_b = [2 * (d * b // 8 + 4 * ng + 2) for b in cfg.res_bits[: L - 1]]
-    th = B * w.H * ctx                                   # token-heads of one layer
-    io_b = w.q.numel() * 2 + w.pending.numel() * 2 + out.numel() * 2
-    bytes_multi = th * (ref_b + sum(res_b)) + io_b
-    bytes_per = th * (L * ref_b + sum(res_b)) + io_b
-    bytes_bf16 = th * L * 2 * d * 2 + io_b
     kvtok = B * ctx * L                                  # per layer
-    hbm, peak_kind = _peaks()
-
-    def med(x):
-        return statistics.median(x)
-
-    dec_ms = med(t_dec)
-    gbs = bytes_multi / (dec_ms * 1e-3) / 1e9
-    breakdown = {
-        "rq_decode_multiloop": {"ms": dec_ms, "kv_tokens_s": kvtok / (dec_ms * 1e-3),
-                                "gbs": gbs, "frac_hbm_measured": gbs / hbm,
-                                "frac_hbm_nominal_8tbs": gbs / 8000.0},
-        "rq_decode_perloop": {"ms": med(t_per), "kv_tokens_s": kvtok / (med(t_per) * 1e-3),
-                              "gbs": bytes_per / (med(t_per) * 1e-3) / 1e9,
-                              "frac_hbm_measured": bytes_per / (med(t_per) * 1e-3) / 1e9 / hbm},
-        "encode_append_us": 1e3 * med(t_enc),
-    }
-    if t_bf_multi:
-        for name, tt in (("bf16_decode_multiloop", t_bf_multi), ("bf16_decode_perloop", t_bf_per)):
-            m = med(tt)
-            breakdown[name] = {"ms": m, "kv_tokens_s": kvtok / (m * 1e-3),
-                               "gbs": bytes_bf16 / (m * 1e-3) / 1e9,
-                               "frac_hbm_measured": bytes_bf16 / (m * 1e-3) / 1e9 / hbm}
-        breakdown["speedup_vs_bf16"] = {"multiloop": med(t_bf_multi) / dec_ms,
-                                        "perloop": med(t_bf_per) / med(t_per)}
-    breakdown["storage_reduction_vs_bf16"] = 1 - (ref_b + sum(res_b)) / (L * 2 * d * 2)
-    m = med(t_srv)
-    breakdown["serving_step"] = {
-        "what": "per-loop decode of all %d loops + encode of the token + ctx advance, one CUDA "
-                "graph replayed %d times (ctx %d..%d)" % (L, len(t_srv), ctx, ctx + grown),
-        "ms": m, "tokens_s": B / (m * 1e-3), "kv_tokens_s": kvtok / (m * 1e-3)}
-    m = med(t_pre)
-    breakdown["prefill_encode"] = {
-        "what": "rq_encode_append of %d tokens x %d sequences in one call" % (n_pre, B),
-        "ms": m, "tokens_s": B * n_pre / (m * 1e-3),
-        "gbs": (pre_bytes + B * n_pre * w.H * (ref_b + sum(res_b))) / (m * 1e-3) / 1e9}
-    if t_pg_multi:
-        for name, tt, nb, base in (("rq_paged_decode_multiloop", t_pg_multi, bytes_multi, dec_ms),
-                                   ("rq_paged_decode_perloop", t_pg_per, bytes_per, med(t_per))):
-            m = med(tt)
-            breakdown[name] = {"ms": m, "kv_tokens_s": kvtok / (m * 1e-3),
-                               "gbs": nb / (m * 1e-3) / 1e9,
-                               "frac_hbm_measured": nb / (m * 1e-3) / 1e9 / hbm,
-                               "time_vs_contiguous": m / base}
-
+    dec = breakdown["rq_decode_multiloop"]
     value = kvtok * NL * world / (ms * 1e-3)
+    del layers, outs, out, out1, w, g_step, ws, ws1, ws_srv
+    torch.cuda.empty_cache()
+
+    # ---- every other workload and the fixed-budget experiment, measured in this run ----
+    if world == 1 and not args.no_sweep:
+        import synth
+        per = {}
+        for other in synth.CONFIGS:
+            if other.name != cfg.name:
+                per[other.name] = sweep_workload(other.name, iters, hbm)
+        breakdown["per_workload"] = per
+    if world == 1 and args.budget_gb > 0:
+        breakdown["budget"] = budget_experiment(args.budget_workload, args.budget_gb,
+                                                max(10, args.steps))
+
     line = {
         "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -448,11 +611,13 @@ def gpu_arm(args, cfg):
                    "deferred-write encode/append of the current token (CUDA graph replay)",
                    "layers_timed": NL,
                    "l2": "inputs larger than L2 (%.0f MB packed cache read per step)" %
-                   (bytes_multi / 1e6), "parallelism": "replicas (weak, per-GPU batch %d)" % B},
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "traffic": _traffic(cfg.name), "peak_kind": peak_kind,
-                     "kernel": "rq_decode_attention (split kernel + combine, timed per call)",
-                     "algorithmic_bytes_per_launch": bytes_multi},
+                   (nb["multi"] / 1e6), "parallelism": "replicas (weak, per-GPU batch %d)" % B},
+        "roofline": {"bound": "hbm", "achieved": dec["gbs"], "peak": hbm, "unit": "GB/s",
+                     "frac": dec["gbs"] / hbm, "traffic": _traffic(cfg.name),
+                     "peak_kind": peak_kind,
+                     "kernel": "rq_decode_attention all-loops call (split kernel + combine, "
+                               "timed per call)",
+                     "algorithmic_bytes_per_launch": nb["multi"]},
         "cpu_baseline": cpu,
         "e2e": {"value": kvtok * NL * world / (t_e2e * 1e-3), "unit": "KV tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -466,90 +631,25 @@ def gpu_arm(args, cfg):
         dist.destroy_process_group()
 
 
-def budget_arm(args, cfg):
-    """Fixed KV-memory budget per layer: the largest batch whose cache fits, for the packed
-    cache and for the BF16 cache, and decode KV tokens/s of each at its own batch (one JSON
-    line)."""
-    import torch
-
-    import looped_transformer_kv_gb300 as rqm
-    from looped_transformer_kv_gb300.workload import Workload
-
-    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-    budget = int(args.budget_gb * (1 << 30))
-    cap = max(64, -(-(cfg.ctx + 2) // 64) * 64)
-    L, H, d = cfg.n_loops, cfg.n_kv_heads, cfg.head_dim
-    rq_seq = rqm.rq.cache_bytes(rqm.make_shape(1, cfg.n_q_heads, H, d, L, cap,
-                                               cfg.res_bits[: L - 1]))
-    bf_seq = 2 * H * L * cap * d * 2
-    res = {"experiment": "fixed KV-memory budget per layer", "workload": _workload_desc(cfg),
-           "budget_gib": args.budget_gb, "bytes_per_sequence": {"rq": rq_seq, "bf16": bf_seq}}
-    iters = max(args.steps, 10)
-
-    def timed(fn):
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            fn()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr):
-            fn()
-        for _ in range(max(3, args.warmup)):
-            gr.replay()
-        torch.cuda.synchronize()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        ev[0].record()
-        for _ in range(iters):
-            gr.replay()
-        ev[1].record()
-        torch.cuda.synchronize()
-        return ev[0].elapsed_time(ev[1]) / iters
-
-    for kind in ("rq", "bf16"):
-        B = budget // (rq_seq if kind == "rq" else bf_seq)
-        w = Workload(cfg, capacity=cap, batch=int(B), build_rq=kind == "rq",
-                     build_bf16=kind == "bf16")
-        out, ws = w.out_buffer(L), w.workspace(L)
-        out1, ws1 = [w.out_buffer(1) for _ in range(L)], w.workspace(1)
-        dec = w.decode if kind == "rq" else w.decode_bf16
-        t_multi = timed(lambda: dec(0, L, out, ws))
-
-        def per():
-            for l in range(L):
-                dec(l, 1, out1[l], ws1)
-
-        t_per = timed(per)
-        kvtok = B * cfg.ctx * L
-        res[kind] = {"batch": int(B), "cache_gib": B * (rq_seq if kind == "rq" else bf_seq) / 2**30,
-                     "multiloop_ms": t_multi, "multiloop_kv_tokens_s": kvtok / (t_multi * 1e-3),
-                     "perloop_ms": t_per, "perloop_kv_tokens_s": kvtok / (t_per * 1e-3)}
-        del w, out, ws, out1, ws1
-        torch.cuda.empty_cache()
-    res["batch_ratio"] = res["rq"]["batch"] / res["bf16"]["batch"]
-    res["throughput_ratio_multiloop"] = (res["rq"]["multiloop_kv_tokens_s"] /
-                                         res["bf16"]["multiloop_kv_tokens_s"])
-    res["throughput_ratio_perloop"] = (res["rq"]["perloop_kv_tokens_s"] /
-                                       res["bf16"]["perloop_kv_tokens_s"])
-    print(json.dumps(res), flush=True)
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="layer_1p4b")
+    ap.add_argument("--workload", default="serving")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-paged", action="store_true")
-    ap.add_argument("--budget-gb", type=float, default=0.0,
-                    help="run the fixed KV-memory budget experiment (GiB per layer) instead")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the other workloads and the budget experiment")
+    ap.add_argument("--budget-gb", type=float, default=8.0,
+                    help="fixed KV-memory budget per layer (GiB) of the budget experiment; 0: skip")
+    ap.add_argument("--budget-workload", default="layer_1p4b")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.no_sweep:
+        args.budget_gb = 0.0
     import synth
     cfg = synth.config_by_name(args.workload)
     if args.impl == "reference":
@@ -557,10 +657,7 @@ def main():
     else:
         from __graft_entry__ import build
         build()
-        if args.budget_gb > 0:
-            budget_arm(args, cfg)
-        else:
-            gpu_arm(args, cfg)
+        gpu_arm(args, cfg)
 
 
 if __name__ == "__main__":
