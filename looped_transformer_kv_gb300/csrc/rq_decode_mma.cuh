@@ -26,7 +26,9 @@
 // A pair of packed codes becomes an f16x2 operand with one AND (scores: the masked bits are
 // the fp16 subnormal c * 2^-24 times a power of two fixed by their bit position, folded into
 // the query fragments, with 2^24 restored in fp32) or with an OR and a packed subtraction
-// (values: exact normal fp16 code times a power of two removed per output row at the end).
+// (values: exact normal fp16 code times a power of two removed per output row at the end, for
+// 4-bit codes; 2-bit residual codes are subnormal like the score operands, with 2^24 and the
+// bit position's power of two removed per output row at the end).
 // The other operand (queries, softmax weights) is split into an fp16 high part and an fp16
 // low part (two MMAs; for blocks of at most 4 query columns one MMA, the low parts riding in
 // the 4 free columns; for a single query column the columns carry its channel groups) and so
@@ -991,8 +993,8 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
 #pragma unroll
               for (int mtg = 0; mtg < 2; ++mtg) {
                 uint32_t x0, x1, x2, x3;
-                a_pairs_2bit<true>(W0, mtg, x0, x1);
-                a_pairs_2bit<true>(W1, mtg, x2, x3);
+                a_pairs_2bit(W0, mtg, x0, x1);
+                a_pairs_2bit(W1, mtg, x2, x3);
                 mma_f16(accE2[2 * g + mtg], x0, x1, x2, x3, g0, g1);
               }
             } else if (RES4) {
@@ -1114,8 +1116,8 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
 #pragma unroll
                 for (int mtg = 0; mtg < 2; ++mtg) {
                   uint32_t x0, x1, x2, x3;
-                  a_pairs_2bit<true>(W0, mtg, x0, x1);
-                  a_pairs_2bit<true>(W1, mtg, x2, x3);
+                  a_pairs_2bit(W0, mtg, x0, x1);
+                  a_pairs_2bit(W1, mtg, x2, x3);
                   mma_f16(accE2[2 * g + mtg], x0, x1, x2, x3, eh0, eh1);
                   if (!HL) mma_f16(accE2[2 * g + mtg], x0, x1, x2, x3, el0, el1);
                 }
@@ -1233,7 +1235,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
       for (int j = 0; j < 4; ++j) {
         const int mtg = j >> 1, hh = j & 1, k = 2 * hh + e;
         const float sc4 = hh ? 0.0625f : 1.f;
-        const float sc2 = 1.f / float(1 << (2 * j));
+        const float sc2 = 16777216.f / float(1 << (2 * j));   // 2-bit codes: subnormal
         vr[j] = fmaf(accR[2 * g + mtg][k], sc4, offR[0][e]) * f[e];
         float x = fmaf(accE2[2 * g + mtg][k], sc2, offE[0][e]);
         if (RES4) x = fmaf(accE4[RES4 ? 2 * g + mtg : 0][k], sc4, x);
@@ -1256,7 +1258,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
       for (int j = 0; j < 4; ++j) {
         const int mtg = j >> 1, hh = j & 1, k = 2 * hh + e;
         const float sc4 = hh ? 0.0625f : 1.f;     // value codes are normal fp16
-        const float sc2 = 1.f / float(1 << (2 * j));
+        const float sc2 = 16777216.f / float(1 << (2 * j));   // 2-bit codes: subnormal
         vr[j] = fmaf(accR[2 * g + mtg][k], sc4, offR[g][e]) * f[e];
         float x = fmaf(accE2[2 * g + mtg][k], sc2, offE[g][e]);
         if (RES4) x = fmaf(accE4[RES4 ? 2 * g + mtg : 0][k], sc4, x);
