@@ -10,7 +10,8 @@ The headline workload is the serving-scale one (B 128, ctx 32768, 16 heads, d 12
 decode and deferred-write encode interleaved in a step).  The line's `breakdown` also carries,
 measured in the same run, every other workload (per-layer times, all 24 layers for mixed_24l),
 the BF16 comparison kernel on the same shapes, the paged cache, the serving step under a CUDA
-graph, the bulk prefill encode and the fixed KV-memory budget experiment.
+graph, the bulk prefill encode, the fixed KV-memory budget experiment and the ablation rows
+(per-loop throughput of the method with a fixed at 1 and of direct quantisation).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
                 [--no-sweep] [--no-bf16] [--no-paged] [--no-cpu-baseline] [--budget-gb G]
@@ -426,6 +427,46 @@ def budget_experiment(name, budget_gib, iters):
     return res
 
 
+def ablation_rows(name, iters, hbm):
+    """Ablation rows of the method's steps (include/rq_ablation.h), on one workload: each
+    variant's cache is encoded with its own a (least squares / 1 / 0) and decoded by causal
+    per-loop calls (loop l < L-1 by the variant's kernel, the final loop, the INT4 reference,
+    by the method's kernel); bytes are what each variant's decode reads."""
+    import torch
+
+    import synth
+    from looped_transformer_kv_gb300.workload import Workload
+    cfg = synth.config_by_name(name)
+    L, d = cfg.n_loops, cfg.head_dim
+    ng = d // 32
+    ref_b = 2 * (d // 2 + 4 * ng)
+    res_b = [2 * (d * b // 8 + 4 * ng) for b in cfg.res_bits[: L - 1]]   # codes + step/offset
+    rows = {"workload": _workload_desc(cfg),
+            "what": "all L loops as causal per-loop calls; bytes = what each decode reads"}
+    med = statistics.median
+    for variant, mode in (("rq", 0), ("a_one", 1), ("direct_rotated", 2)):
+        w = Workload(cfg, capacity=cfg.ctx + 2, alpha_mode=mode)
+        outs = [w.out_buffer(1) for _ in range(L)]
+        ws1 = w.workspace(1)
+
+        def per():
+            for l in range(L):
+                if mode == 0 or l == L - 1:
+                    w.decode(l, 1, outs[l], ws1)
+                else:
+                    w.decode_ablation(l, outs[l], ws1)
+
+        t = med(timeit(graph_of(per), iters))
+        a_b = 0 if mode else 4                               # the a stream (K and V)
+        per_th = sum((ref_b if mode != 2 else 0) + rb + a_b for rb in res_b) + ref_b
+        th = w.B * w.H * cfg.ctx
+        nbytes = th * per_th + w.q.numel() * 2 + w.pending.numel() * 2 + outs[0].numel() * 2 * L
+        rows[variant] = dict(_row(t, w.B * cfg.ctx * L, nbytes, hbm), bytes_per_token_head=per_th)
+        del w, outs, ws1
+        torch.cuda.empty_cache()
+    return rows
+
+
 def gpu_arm(args, cfg):
     import torch
     import torch.distributed as dist
@@ -598,6 +639,8 @@ def gpu_arm(args, cfg):
             if other.name != cfg.name:
                 per[other.name] = sweep_workload(other.name, iters, hbm)
         breakdown["per_workload"] = per
+    if world == 1 and not args.no_sweep:
+        breakdown["ablation"] = ablation_rows("layer_1p4b", iters, hbm)
     if world == 1 and args.budget_gb > 0:
         breakdown["budget"] = budget_experiment(args.budget_workload, args.budget_gb,
                                                 max(10, args.steps))

@@ -1,4 +1,5 @@
-"""ctypes declarations of librq's C ABI (include/rq.h, include/rq_synth.h, include/rq_test.h).
+"""ctypes declarations of librq's C ABI (include/rq.h, include/rq_synth.h, include/rq_test.h,
+include/rq_ablation.h).
 
 Loading fails loudly: there is no fallback implementation of any entry point.
 """
@@ -17,7 +18,8 @@ EXPORTS = ("rq_cache_bytes", "rq_encode_append", "rq_decode_workspace_bytes",
            "rq_synth_states", "rq_synth_queries", "rq_decode_noalloc_scratch_bytes",
            "rq_decode_attention_noalloc", "rq_paged_cache_bytes", "rq_paged_encode_append",
            "rq_paged_decode_attention", "rq_advance_ctx",
-           "rq_test_decode_attention_wait_runs_out")
+           "rq_test_decode_attention_wait_runs_out", "rq_ablation_encode_append",
+           "rq_ablation_decode_attention")
 
 
 class RqShape(ctypes.Structure):
@@ -93,6 +95,10 @@ def lib():
     L.rq_test_decode_attention_wait_runs_out.argtypes = [S, C, _P, i32, i32, _P, _P, i32, _P,
                                                          _P, sz, ctypes.c_uint64, _P]
     L.rq_test_decode_attention_wait_runs_out.restype = i32
+    L.rq_ablation_encode_append.argtypes = [S, C, _P, ctypes.POINTER(i64), _P, i32, i32, i32, _P]
+    L.rq_ablation_encode_append.restype = i32
+    L.rq_ablation_decode_attention.argtypes = [S, C, i32, _P, i32, _P, _P, i32, _P, _P, sz, _P]
+    L.rq_ablation_decode_attention.restype = i32
     L.rq_advance_ctx.argtypes = [_P, i32, i32, i32, _P]
     L.rq_advance_ctx.restype = i32
     L.rq_status_str.argtypes = [i32]

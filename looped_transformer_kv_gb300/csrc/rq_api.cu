@@ -3,6 +3,7 @@
 #include <cmath>
 #include <new>
 
+#include "../../include/rq_ablation.h"
 #include "../../include/rq_test.h"
 #include "rq_common.cuh"
 #include "rq_kernels.h"
@@ -90,7 +91,7 @@ size_t token_head_bytes(const rq_shape* s) {
 rq_status encode_common(const rq_shape* shape, const rq_cache* cache, const rq_paging* paging,
                         const uint16_t* kv_new, const int64_t strides[5],
                         const int32_t* positions, int32_t pos_begin, int32_t n_new,
-                        void* stream) {
+                        void* stream, int alpha_mode = 0) {
   rq_status st = check_shape(shape);
   if (st != RQ_OK) return st;
   if ((st = check_cache(shape, cache)) != RQ_OK) return st;
@@ -103,7 +104,8 @@ rq_status encode_common(const rq_shape* shape, const rq_cache* cache, const rq_p
   if (n_new == 0) return RQ_OK;
   try {
     return from_cuda(rq::launch_encode(*shape, *cache, paging, kv_new, strides, positions,
-                                       pos_begin, n_new, static_cast<cudaStream_t>(stream)));
+                                       pos_begin, n_new, static_cast<cudaStream_t>(stream),
+                                       alpha_mode));
   } catch (...) {
     return RQ_ERR_INTERNAL;
   }
@@ -234,6 +236,36 @@ rq_status rq_test_decode_attention_wait_runs_out(const rq_shape* shape, const rq
   const rq::DecodeHooks hooks{wait_limit_ns, true};
   return decode_common(shape, cache, nullptr, q, loop_begin, loop_count, pending_kv, ctx_lens,
                        max_ctx, out, ws, ws_bytes, stream, &hooks);
+}
+
+rq_status rq_ablation_encode_append(const rq_shape* shape, const rq_cache* cache,
+                                    const uint16_t* kv_new, const int64_t strides[5],
+                                    const int32_t* positions, int32_t pos_begin, int32_t n_new,
+                                    int32_t alpha_mode, void* stream) {
+  if (alpha_mode < RQ_ALPHA_LEAST_SQUARES || alpha_mode > RQ_ALPHA_ZERO) return RQ_ERR_INVALID_ARG;
+  return encode_common(shape, cache, nullptr, kv_new, strides, positions, pos_begin, n_new,
+                       stream, alpha_mode);
+}
+
+rq_status rq_ablation_decode_attention(const rq_shape* shape, const rq_cache* cache, int32_t mode,
+                                       const uint16_t* q, int32_t loop, const uint16_t* pending_kv,
+                                       const int32_t* ctx_lens, int32_t max_ctx, uint16_t* out,
+                                       void* ws, size_t ws_bytes, void* stream) {
+  rq_status st = check_shape(shape);
+  if (st != RQ_OK) return st;
+  if ((st = check_cache(shape, cache)) != RQ_OK) return st;
+  if (mode != RQ_ALPHA_ONE && mode != RQ_ALPHA_ZERO) return RQ_ERR_INVALID_ARG;
+  if (loop < 0 || loop >= shape->n_loops - 1) return RQ_ERR_INVALID_ARG;
+  if ((st = check_decode(shape, q, loop, 1, ctx_lens, max_ctx, out, ws, ws_bytes)) != RQ_OK)
+    return st;
+  if (shape->n_q_heads != shape->n_kv_heads || shape->head_dim != 128) return RQ_ERR_UNSUPPORTED;
+  try {
+    return from_cuda(rq::launch_rq_ablation_decode(*shape, *cache, mode, q, loop, pending_kv,
+                                                   ctx_lens, max_ctx, out, static_cast<float*>(ws),
+                                                   static_cast<cudaStream_t>(stream)));
+  } catch (...) {
+    return RQ_ERR_INTERNAL;
+  }
 }
 
 rq_status rq_advance_ctx(int32_t* ctx_lens, int32_t batch, int32_t n, int32_t capacity,

@@ -242,4 +242,106 @@ cudaError_t launch_rq_decode_mma(const rq_shape& s, const rq_cache& cache, const
   return cudaSuccess;
 }
 
+// ---------------------------------------------------------------------------- ablation rows
+// Per-loop calls with one query column per kv-head and head dim 128 over a cache encoded with
+// a fixed at 1 (mode 1, no a stream read) or at 0 (mode 2: the loop's own rotated INT2/INT4
+// codes, no reference read): the single-column kernel with the reference and/or the a stream
+// left out of its stage.
+
+namespace {
+
+template <int MODE>
+KernelFn pick_mode(bool res4) {
+  return res4 ? rq_mma_kernel<128, true, 1, false, 2, MODE> : rq_mma_kernel<128, false, 1, false, 2, MODE>;
+}
+
+}  // namespace
+
+cudaError_t launch_rq_ablation_decode(const rq_shape& s, const rq_cache& cache, int mode,
+                                      const uint16_t* q, int loop, const uint16_t* pending,
+                                      const int32_t* ctx_lens, int max_ctx, uint16_t* out,
+                                      float* ws, cudaStream_t stream) {
+  const KernelFn fn = mode == 1 ? pick_mode<1>(s.res_bits[loop] == 4) : pick_mode<2>(s.res_bits[loop] == 4);
+  const int D = 128, NG = 4;
+  const int bits = s.res_bits[loop];
+  MmaArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kc = cache.ref_codes[0];
+  a.km = cache.ref_meta[0];
+  a.vc = cache.ref_codes[1];
+  a.vm = cache.ref_meta[1];
+  int off = 0;
+  if (mode != 2) {
+    a.off_kc = off; off += kT * D / 2;
+    a.off_km = off; off += kT * NG * 4;
+    a.off_vc = off; off += kT * D / 2;
+    a.off_vm = off; off += kT * NG * 4;
+  }
+  a.rbits[0] = bits;
+  a.krc[0] = cache.res_codes[0][loop];
+  a.krm[0] = cache.res_meta[0][loop];
+  a.vrc[0] = cache.res_codes[1][loop];
+  a.vrm[0] = cache.res_meta[1][loop];
+  a.off_krc[0] = off; off += kT * D * bits / 8;
+  a.off_krm[0] = off; off += kT * NG * 4;
+  a.off_vrc[0] = off; off += kT * D * bits / 8;
+  a.off_vrm[0] = off; off += kT * NG * 4;
+  a.stage_bytes = off;
+  a.qrm_bytes = 0;
+  QueryBlock bq;
+  bq.gi0 = 0; bq.gw = 1; bq.lb = loop; bq.nl = 1; bq.r0 = loop; bq.nr = 1;
+  a.blk = bq;
+  // the method's split plan for this per-loop call (the workspace is sized for it)
+  const SplitPlan plan = plan_splits_rq(s, loop, 1, max_ctx);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  size_t smem = 0;
+  int best = 0;
+  for (int stages = 3; stages >= 2; --stages) {
+    const size_t sm = smem_layout(D, bits == 4, stages, a.stage_bytes, 0, 0).total;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kW * 32, sm) != cudaSuccess) n = 0;
+    if (n > best) {
+      best = n;
+      a.n_stages = stages;
+      smem = sm;
+    }
+  }
+  if (best == 0) return cudaErrorInvalidConfiguration;
+  unsigned* err = reinterpret_cast<unsigned*>(ws);
+  const size_t tb = ws_ticket_bytes(s, 1);
+  unsigned* tickets = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + kWsHeaderBytes);
+  float* part = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + kWsHeaderBytes + tb);
+  e = cudaMemsetAsync(ws, 0, kWsHeaderBytes + tb, stream);
+  if (e != cudaSuccess) return e;
+  a.ksigns = cache.rot_signs[0];
+  a.vsigns = cache.rot_signs[1];
+  a.q = q;
+  a.ctx_lens = ctx_lens;
+  a.part = part;
+  a.err = err;
+  a.pending = pending;
+  a.out = out;
+  a.tickets = tickets;
+  a.B = s.batch;
+  a.Hq = s.n_q_heads;
+  a.H = s.n_kv_heads;
+  a.L = s.n_loops;
+  a.cap = s.capacity;
+  a.g = 1;
+  a.loop_begin = loop;
+  a.loop_count = 1;
+  a.n_splits = plan.n_splits;
+  a.tokens_per_split = plan.tokens_per_split;
+  const float scale = s.softmax_scale > 0.f ? s.softmax_scale : 1.0f / sqrtf(float(s.head_dim));
+  a.scale_log2 = scale * kLog2e;
+  a.wait_limit_ns = kWaitLimitNs;
+  dim3 grid(plan.n_splits, s.n_kv_heads, s.batch);
+  fn<<<grid, kW * 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace rq

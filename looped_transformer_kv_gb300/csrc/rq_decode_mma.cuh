@@ -218,7 +218,10 @@ __device__ __forceinline__ void weights_to_b_packed(float w00, float w01, float 
 // every lane of a fragment row scales distinct groups and one transpose serves every group.
 // Blocks of the final loop alone (NRT 0) and single-column blocks with a 2-bit residual loop
 // are held to 128 registers for four resident CTAs per SM; the others take up to 168 for three.
-template <int D, bool RES4, int NRT, bool PAGED, int PK>
+// MODE (ablation rows of the method's steps; single-column blocks of one residual loop only):
+// 0 = the method; 1 = a fixed at 1 (no a stream is read); 2 = direct quantisation of the loop
+// (no reference is read: the score and the value are the loop's own codes alone, a = 0).
+template <int D, bool RES4, int NRT, bool PAGED, int PK, int MODE = 0>
 __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 : 3) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NG = D / 32;
   constexpr int NQ = kNQ;
@@ -233,6 +236,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   // rotated-query fragments masked to its columns (no per-loop accumulator to select from)
   constexpr bool MASKB = PK == 1 && !RES4 && PER_LOOP && NRT >= 2;
   static_assert(!SC || (NRT == 0 || NRT == 1) && D == 128, "single-column blocks: D 128, one loop");
+  static_assert(MODE == 0 || (SC && NRT == 1 && !PAGED), "ablation modes: single-column, one loop");
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   // residual loop K codes, K steps, K a, V codes, V steps, V a.  Fixed at compile time when
   // the residual-loop count is and every residual loop is 2-bit (for up to two residual
   // loops: with three, the constant addresses cost more registers than they save).
-  constexpr bool FIXED = !RES4 && NRT >= 0 && NRT <= 2;
+  constexpr bool FIXED = MODE == 0 && !RES4 && NRT >= 0 && NRT <= 2;
   constexpr int F_KM = kT * RB4, F_VC = F_KM + kT * NG * 4, F_VM = F_VC + kT * RB4;
   constexpr int F_RES = F_VM + kT * NG * 4;
   constexpr int F_KRM = kT * RB2, F_KA = F_KRM + kT * NG * 4, F_VRC = F_KA + kT * 2;
@@ -364,20 +368,22 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
     const int64_t tok = paged ? (int64_t(pid[tile]) * a.H + h) * kT
                               : slot * a.cap + t_begin + int64_t(tile) * kT;
     mbar_arrive_expect_tx(bar, uint32_t(a.stage_bytes));
-    bulk_g2s(dst + a.off_kc, a.kc + tok * RB4, kT * RB4, bar);
-    bulk_g2s(dst + a.off_km, a.km + tok * NG * 2, kT * NG * 4, bar);
-    bulk_g2s(dst + a.off_vc, a.vc + tok * RB4, kT * RB4, bar);
-    bulk_g2s(dst + a.off_vm, a.vm + tok * NG * 2, kT * NG * 4, bar);
+    if constexpr (MODE != 2) {
+      bulk_g2s(dst + a.off_kc, a.kc + tok * RB4, kT * RB4, bar);
+      bulk_g2s(dst + a.off_km, a.km + tok * NG * 2, kT * NG * 4, bar);
+      bulk_g2s(dst + a.off_vc, a.vc + tok * RB4, kT * RB4, bar);
+      bulk_g2s(dst + a.off_vm, a.vm + tok * NG * 2, kT * NG * 4, bar);
+    }
 #pragma unroll
     for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
       if (ri >= nr) break;
       const int rb = (!RES4 || a.rbits[ri] == 2) ? RB2 : RB4;
       bulk_g2s(dst + a.off_krc[ri], a.krc[ri] + tok * rb, kT * rb, bar);
       bulk_g2s(dst + a.off_krm[ri], a.krm[ri] + tok * NG * 2, kT * NG * 4, bar);
-      bulk_g2s(dst + a.off_ka[ri], a.ka[ri] + tok, kT * 2, bar);
+      if (MODE == 0) bulk_g2s(dst + a.off_ka[ri], a.ka[ri] + tok, kT * 2, bar);
       bulk_g2s(dst + a.off_vrc[ri], a.vrc[ri] + tok * rb, kT * rb, bar);
       bulk_g2s(dst + a.off_vrm[ri], a.vrm[ri] + tok * NG * 2, kT * NG * 4, bar);
-      bulk_g2s(dst + a.off_va[ri], a.va[ri] + tok, kT * 2, bar);
+      if (MODE == 0) bulk_g2s(dst + a.off_va[ri], a.va[ri] + tok, kT * 2, bar);
     }
   };
   if (threadIdx.x == 0) {   // the barriers' initialisation is ordered before by the fence
@@ -617,19 +623,21 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
       if constexpr (SC) {
         // one accumulator for every group: column n holds group n & 3 (n >= 4: low parts)
         float D0[4] = {0.f, 0.f, 0.f, 0.f}, Dr[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t kw0[NG], kw1[NG];
-        load_words<NG>(sb + o_kc + tr0 * RB4 + c * NG * 4, kw0);
-        load_words<NG>(sb + o_kc + tr1 * RB4 + c * NG * 4, kw1);
+        if constexpr (MODE != 2) {
+          uint32_t kw0[NG], kw1[NG];
+          load_words<NG>(sb + o_kc + tr0 * RB4 + c * NG * 4, kw0);
+          load_words<NG>(sb + o_kc + tr1 * RB4 + c * NG * 4, kw1);
 #pragma unroll
-        for (int gq = 0; gq < NG; ++gq)
+          for (int gq = 0; gq < NG; ++gq)
 #pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            uint32_t a0, a2, a1, a3;
-            a_pairs_4bit(kw0[gq], s, a0, a2);
-            a_pairs_4bit(kw1[gq], s, a1, a3);
-            const uint2 bq = *reinterpret_cast<const uint2*>(&QF[(gq * 2 + s) * 32 + lane]);
-            mma_f16(D0, a0, a1, a2, a3, bq.x, bq.y);
-          }
+            for (int s = 0; s < 2; ++s) {
+              uint32_t a0, a2, a1, a3;
+              a_pairs_4bit(kw0[gq], s, a0, a2);
+              a_pairs_4bit(kw1[gq], s, a1, a3);
+              const uint2 bq = *reinterpret_cast<const uint2*>(&QF[(gq * 2 + s) * 32 + lane]);
+              mma_f16(D0, a0, a1, a2, a3, bq.x, bq.y);
+            }
+        }
         if (NRT == 1) {   // the block's residual loop
           const bool two = !RES4 || a.rbits[0] == 2;
 #pragma unroll
@@ -661,10 +669,10 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
           }
         }
         // step and offset of this lane's two groups for tokens tr0 and tr1
-        const uint2 m0 = *reinterpret_cast<const uint2*>(sb + o_km + (tr0 * NG + gp) * 4);
-        const uint2 m1 = *reinterpret_cast<const uint2*>(sb + o_km + (tr1 * NG + gp) * 4);
-        float x[4];
-        {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (MODE != 2) {
+          const uint2 m0 = *reinterpret_cast<const uint2*>(sb + o_km + (tr0 * NG + gp) * 4);
+          const uint2 m1 = *reinterpret_cast<const uint2*>(sb + o_km + (tr1 * NG + gp) * 4);
           const float2 s00 = meta_f2(m0.x), s01 = meta_f2(m0.y);
           const float2 s10 = meta_f2(m1.x), s11 = meta_f2(m1.y);
           x[0] = fmaf(s00.x, D0[0], s00.y * qsS[0]);
@@ -675,7 +683,11 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
         if (NRT == 1) {   // a_t * reference part + residual part
           const uint2 r0 = *reinterpret_cast<const uint2*>(sb + krmD[0] + (tr0 * NG + gp) * 4);
           const uint2 r1 = *reinterpret_cast<const uint2*>(sb + krmD[0] + (tr1 * NG + gp) * 4);
-          const float al0 = ld_half(sb + kaD[0] + tr0 * 2), al1 = ld_half(sb + kaD[0] + tr1 * 2);
+          float al0 = 1.f, al1 = 1.f;   // (MODE 1: a = 1; MODE 2: no reference part)
+          if constexpr (MODE == 0) {
+            al0 = ld_half(sb + kaD[0] + tr0 * 2);
+            al1 = ld_half(sb + kaD[0] + tr1 * 2);
+          }
           const float2 t00 = meta_f2(r0.x), t01 = meta_f2(r0.y);
           const float2 t10 = meta_f2(r1.x), t11 = meta_f2(r1.y);
           x[0] = fmaf(al0, x[0], fmaf(t00.x, Dr[0], t00.y * qrsS[0]));
@@ -930,11 +942,16 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
         if (NRT == 1) {
           pe0 = p[0];
           pe1 = p[2];
-          pa0 *= ld_half(sb + vaD[0] + tr0 * 2);
-          pa1 *= ld_half(sb + vaD[0] + tr1 * 2);
+          if constexpr (MODE == 0) {
+            pa0 *= ld_half(sb + vaD[0] + tr0 * 2);
+            pa1 *= ld_half(sb + vaD[0] + tr1 * 2);
+          }
         }
-        uint2 n0 = *reinterpret_cast<const uint2*>(sb + o_vm + (tr0 * NG + gp) * 4);
-        uint2 n1 = *reinterpret_cast<const uint2*>(sb + o_vm + (tr1 * NG + gp) * 4);
+        uint2 n0 = make_uint2(0u, 0u), n1 = make_uint2(0u, 0u);
+        if constexpr (MODE != 2) {
+          n0 = *reinterpret_cast<const uint2*>(sb + o_vm + (tr0 * NG + gp) * 4);
+          n1 = *reinterpret_cast<const uint2*>(sb + o_vm + (tr1 * NG + gp) * 4);
+        }
         if (partial) {   // rows past the context: zero weights and steps whatever the slots hold
           pa0 = v0 ? pa0 : 0.f;
           pa1 = v1 ? pa1 : 0.f;
@@ -943,7 +960,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
           n0 = v0 ? n0 : make_uint2(0u, 0u);
           n1 = v1 ? n1 : make_uint2(0u, 0u);
         }
-        {
+        if constexpr (MODE != 2) {   // the reference part
           const float2 u00 = meta_f2(n0.x), u01 = meta_f2(n0.y);
           const float2 u10 = meta_f2(n1.x), u11 = meta_f2(n1.y);
           offR[0][0] = fmaf(pa0, u00.y, fmaf(pa1, u10.y, offR[0][0]));

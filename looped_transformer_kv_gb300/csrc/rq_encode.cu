@@ -23,6 +23,7 @@ struct EncodeArgs {
   const int32_t* bt;     // block table of a paged cache, or null
   int32_t max_pages, n_pages;
   int32_t vec;           // kv_new rows allow one vector load of a lane's channels
+  int32_t alpha_mode;    // 0: least-squares a_l (the method); 1: a = 1; 2: a = 0 (ablations)
 };
 
 // Sum over the VL lanes of a vector.
@@ -215,7 +216,8 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
 #pragma unroll
     for (int q = 0; q < P; ++q) num = fmaf(x[q], ref_hat[q], num);
     num = vec_sum<VL>(num);
-    const float alpha = den > 0.f ? __fdiv_rn(num, den) : 0.f;
+    float alpha = den > 0.f ? __fdiv_rn(num, den) : 0.f;
+    if (a.alpha_mode != 0) alpha = a.alpha_mode == 1 ? 1.f : 0.f;   // (ablation encodes)
     const uint16_t a_bits = float_to_half_bits(alpha);
     const float a_h = half_bits_to_float(a_bits);
     if (hl == 0) a.cache.alpha[kv][l][base + tok] = a_bits;
@@ -250,8 +252,9 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
 cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
                           const uint16_t* kv_new,
                           const int64_t strides[5], const int32_t* positions, int32_t pos_begin,
-                          int32_t n_new, cudaStream_t stream) {
+                          int32_t n_new, cudaStream_t stream, int alpha_mode) {
   EncodeArgs a;
+  a.alpha_mode = alpha_mode;
   a.cache = cache;
   a.kv_new = kv_new;
   a.sb = strides[0];

@@ -111,7 +111,7 @@ size_t partial_floats(const rq_shape& s);  // floats of one partial record
 cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
                           const uint16_t* kv_new,
                           const int64_t strides[5], const int32_t* positions, int32_t pos_begin,
-                          int32_t n_new, cudaStream_t stream);
+                          int32_t n_new, cudaStream_t stream, int alpha_mode = 0);
 
 cudaError_t launch_rq_decode(const rq_shape& s, const rq_cache& cache, const rq_paging* paging,
                              const uint16_t* q,
@@ -128,6 +128,13 @@ cudaError_t launch_combine(const rq_shape& s, const int8_t* v_signs, const uint1
                            int loop_count, const uint16_t* pending, int n_splits,
                            uint16_t* out, const float* part, const unsigned* err,
                            cudaStream_t stream);
+
+// Ablation rows (include/rq_ablation.h): a per-loop decode call over a cache encoded with a
+// fixed at 1 (mode 1) or 0 (mode 2), one query column per kv-head, head dim 128.
+cudaError_t launch_rq_ablation_decode(const rq_shape& s, const rq_cache& cache, int mode,
+                                      const uint16_t* q, int loop, const uint16_t* pending,
+                                      const int32_t* ctx_lens, int max_ctx, uint16_t* out,
+                                      float* ws, cudaStream_t stream);
 
 int device_sm_count();
 

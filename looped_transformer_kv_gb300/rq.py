@@ -142,6 +142,27 @@ def encode_append(shape, cache, kv_new, positions=None, pos_begin=0, stream=None
         int(pos_begin), int(n_new), _stream(stream)))
 
 
+def ablation_encode_append(shape, cache, kv_new, alpha_mode, positions=None, pos_begin=0,
+                           stream=None):
+    """rq_ablation_encode_append (include/rq_ablation.h): a_l fixed by alpha_mode
+    (0 least squares, 1 one, 2 zero)."""
+    assert kv_new.dtype == torch.bfloat16 and kv_new.dim() == 6 and kv_new.stride(5) == 1
+    st = (ctypes.c_int64 * 5)(*[kv_new.stride(i) for i in range(5)])
+    check("rq_ablation_encode_append", _lib.lib().rq_ablation_encode_append(
+        ctypes.byref(shape), ctypes.byref(cache.struct), _ptr(kv_new), st, _ptr(positions),
+        int(pos_begin), int(kv_new.shape[1]), int(alpha_mode), _stream(stream)))
+
+
+def ablation_decode_attention(shape, cache, mode, q, loop, pending_kv, ctx_lens, max_ctx, out, ws,
+                              stream=None):
+    """rq_ablation_decode_attention: per-loop decode of residual loop `loop` over a cache
+    encoded with a = 1 (mode 1) or a = 0 (mode 2)."""
+    check("rq_ablation_decode_attention", _lib.lib().rq_ablation_decode_attention(
+        ctypes.byref(shape), ctypes.byref(cache.struct), int(mode), _ptr(q), int(loop),
+        _ptr(pending_kv), _ptr(ctx_lens), int(max_ctx), _ptr(out), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def decode_workspace_bytes(shape, loop_count, max_ctx):
     return int(_lib.lib().rq_decode_workspace_bytes(ctypes.byref(shape), int(loop_count),
                                                     int(max_ctx)))

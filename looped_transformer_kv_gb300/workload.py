@@ -16,9 +16,10 @@ from . import rq
 
 class Workload:
     def __init__(self, cfg, layer=0, capacity=None, ctx_lens=None, build_rq=True,
-                 build_bf16=False, chunk_tokens=2048, device="cuda", batch=None):
+                 build_bf16=False, chunk_tokens=2048, device="cuda", batch=None, alpha_mode=0):
         self.cfg = cfg
         self.layer = layer
+        self.alpha_mode = alpha_mode     # 0: the method; 1 / 2: a fixed at 1 / 0 (ablations)
         self.device = device
         B = cfg.batch if batch is None else batch
         H, Hq, d, L = cfg.n_kv_heads, cfg.n_q_heads, cfg.head_dim, cfg.n_loops
@@ -70,7 +71,10 @@ class Workload:
                 view = buf[:nb, :nt]
                 sub = rq.make_shape(nb, self.Hq, H, d, L, cap, self.cfg.res_bits[: L - 1])
                 sub_cache = self._sub_cache(b0, nb)
-                rq.encode_append(sub, sub_cache, view, pos_begin=t0)
+                if self.alpha_mode:
+                    rq.ablation_encode_append(sub, sub_cache, view, self.alpha_mode, pos_begin=t0)
+                else:
+                    rq.encode_append(sub, sub_cache, view, pos_begin=t0)
         del buf
 
     def _sub_cache(self, b0, nb):
@@ -117,6 +121,12 @@ class Workload:
                 self.pending[:, :, loop_begin:loop_begin + loop_count].contiguous())
         rq.decode_attention(self.shape, self.cache, q, loop_begin, loop_count, pend,
                             self.ctx_lens, self.max_ctx, out, ws, stream)
+
+    def decode_ablation(self, loop, out, ws, pending=True, stream=None):
+        """Per-loop decode of residual loop `loop` over this (ablation-encoded) cache."""
+        pend = self.pending_loop[loop] if pending else None
+        rq.ablation_decode_attention(self.shape, self.cache, self.alpha_mode, self.q_loop[loop],
+                                     loop, pend, self.ctx_lens, self.max_ctx, out, ws, stream)
 
     def decode_bf16(self, loop_begin, loop_count, out, ws, pending=True, stream=None):
         q = self.q if loop_count == self.L else (

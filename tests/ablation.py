@@ -6,6 +6,7 @@ fails, the LS scale and the rotation each reduce the error; rit.work summary, "H
 pass's KV cache is reconstructed"):
   rq           the method: INT4 final-loop reference, LS scale a_l, rotated residual
   direct       every non-final loop quantised directly at its residual bit width, no reference
+  direct_rotated  the same in the rotated basis (what the GPU ablation kernel decodes)
   no_ls        a_l = 1 (residual against the unscaled reference)
   no_rotation  R = I (residual quantised in original channels)
   chained      loop l's reference is the reconstruction of loop l + 1 (a chain towards the
@@ -62,8 +63,35 @@ def recon_chained(x, signs, res_bits):
     return _residual_loops(x, signs, res_bits, scale=True, rotate=True, chain=True)
 
 
-VARIANTS = {"rq": recon_rq, "direct": recon_direct, "no_ls": recon_no_ls,
-            "no_rotation": recon_no_rotation, "chained": recon_chained}
+def encode_fixed_alpha(x, signs, res_bits, a_value, rnd=O.default_rnd):
+    """The oracle's encode steps with the LS scale replaced by a fixed a (1: residual against
+    the unscaled reference; 0: the loop's own state rotated and quantised directly), with the
+    same rounding hook as oracle.encode so that a GPU encode can be followed code for code."""
+    x = np.asarray(x, dtype=np.float64)
+    L = x.shape[1]
+    R = O.rotation(signs)
+    rc, rs, rz = O.quantize(x[:, L - 1, :], 4, "ref", rnd)
+    ref_hat = O.dequant(rc, rs, rz)
+    out = {"ref": (rc, rs, rz), "alpha": [], "res": []}
+    for l in range(L - 1):
+        a = np.full(x.shape[0], float(a_value))            # exact in fp16
+        a_h = rnd("alpha%d" % l, a, a)
+        y = (x[:, l, :] - a_h[:, None] * ref_hat) @ R.T
+        c, s, z = O.quantize(y, res_bits[l], "res%d" % l, rnd)
+        out["alpha"].append(a_h)
+        out["res"].append((c, s, z))
+    return out
+
+
+def recon_direct_rotated(x, signs, res_bits):
+    """Direct quantisation of every non-final loop in the rotated basis (a = 0): the format the
+    GPU ablation kernel decodes; the rotation costs the decode nothing (one transform of the
+    query and one of the accumulator), so its bytes and time are those of direct INT2."""
+    return O.reconstruct(encode_fixed_alpha(x, signs, res_bits, 0.0), signs)
+
+
+VARIANTS = {"rq": recon_rq, "direct": recon_direct, "direct_rotated": recon_direct_rotated,
+            "no_ls": recon_no_ls, "no_rotation": recon_no_rotation, "chained": recon_chained}
 
 
 def bytes_per_token_head(variant, d, res_bits):
@@ -71,7 +99,7 @@ def bytes_per_token_head(variant, d, res_bits):
     ng = d // 32
     per = d // 2 + 4 * ng                                   # INT4 reference + its meta
     for b in res_bits:
-        per += d * b // 8 + 4 * ng + (0 if variant in ("direct", "no_ls") else 2)
+        per += d * b // 8 + 4 * ng + (0 if variant in ("direct", "direct_rotated", "no_ls") else 2)
     return 2 * per
 
 

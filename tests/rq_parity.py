@@ -162,7 +162,7 @@ def output_errors(gpu, ref):
 
 
 def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True, cache=None,
-                states=None, ctx=None, pending_state=None):
+                states=None, ctx=None, pending_state=None, encode=None):
     """Encode parity and output parity for sequence b, kv-head h of workload w.
 
     loop_calls: list of (loop_begin, loop_count); outs: matching GPU outputs (torch bf16
@@ -172,7 +172,8 @@ def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True, cach
     tokens) passes them: states [n][2][L][d] (n >= ctx: every stored token to check, the
     first ctx of them attended), ctx, and pending_state [2][L][d].  cache: a paged twin
     (PackedCache with n_pages) whose pages hold the slice, read through w's block table
-    argument instead of w's contiguous cache (cache=(paged_cache, table_numpy)).
+    argument instead of w's contiguous cache (cache=(paged_cache, table_numpy)).  encode: the
+    oracle encode to follow (default oracle.encode; an ablation passes its own variant).
     Returns a stats dict; raises AssertionError on a failure.
     """
     cfg, d, L = w.cfg, w.d, w.L
@@ -197,7 +198,7 @@ def check_slice(w, b, h, loop_calls, outs, pending=True, check_encode=True, cach
     encs = []
     for kv in range(2):
         f = Follow(gpu_slice_to_oracle_names(sl, kv, d, L, res_bits))
-        enc = O.encode(x[:, kv], signs[kv], res_bits, rnd=f)
+        enc = (encode or O.encode)(x[:, kv], signs[kv], res_bits, rnd=f)
         assert f.bad == 0, "encode mismatch kv=%d b=%d h=%d: %s" % (kv, b, h, f.bad_names)
         if check_encode:
             assert packed_bytes_equal(enc, sl, kv, res_bits), "packed bytes differ kv=%d" % kv
