@@ -27,22 +27,34 @@
  *     exception crosses the ABI and the library keeps no mutable global state.
  *
  * Packed cache layout (one layer; kv = 0 for K, 1 for V; d = head_dim, ng = d / 32):
- *   ref_codes[kv]     uint8  [B][Hkv][cap][d/2]          INT4 reference codes
- *   ref_meta[kv]      fp16   [B][Hkv][cap][ng][2]        per group (step, offset)
- *   res_codes[kv][l]  uint8  [B][Hkv][cap][d*b_l/8]      residual codes, l < L-1
- *   res_meta[kv][l]   fp16   [B][Hkv][cap][ng][2]
- *   alpha[kv][l]      fp16   [B][Hkv][cap]               least-squares scale a_l
- *   rot_signs[kv]     int8   [Hkv][d]                    +-1; R = H_d diag(signs)/sqrt(d)
+ * one byte array of tile records, [B][Hkv][cap/64] records, one per (sequence, kv-head,
+ * 64-token tile), each rq_record_bytes(shape) = 64 * (token-head bytes) long and made of
+ * sections, each section 64 rows of one kind, in this order:
+ *   reference section:
+ *     K codes  [64][d/2]      INT4 reference codes of K
+ *     K meta   [64][ng][2]    fp16 (step, offset) per group
+ *     V codes  [64][d/2]      INT4 reference codes of V (token-pair order, below)
+ *     V meta   [64][ng][2]
+ *   then one section per non-final loop l = 0 .. L-2 (b_l = residual bits of loop l):
+ *     K codes  [64][d*b_l/8]  residual codes of K
+ *     K meta   [64][ng][2]
+ *     K a      [64]           fp16 least-squares scale a_l of K
+ *     V codes  [64][d*b_l/8]  (token-pair order)
+ *     V meta   [64][ng][2]
+ *     V a      [64]
+ * Row t of a section is token 64 j + t of tile j.  A stage of the decode kernel is one or two
+ * contiguous pieces of a record (the reference section and the sections of the loops it
+ * needs), so each stage moves with one or two bulk copies.  rot_signs[kv] int8 [Hkv][d]:
+ * +-1, R = H_d diag(signs) / sqrt(d).
  * A token's natural code row packs channel i into byte i*b/8 at bit offset (i*b) % 8.
  * K rows store the natural row's 32-bit words group-interleaved: natural word w (the
  * (w % b)-th word of 32-channel group w / b) sits at word (w % b) * (d/32) + w / b.  V rows
- * are stored in token pairs: in pair p (tokens 2p, 2p+1) the 32-bit word at position
- * u ^ swz(p) holds 16-bit unit u of token 2p's natural row (low half) and of token 2p+1's
- * (high half), with swz(p) = 8 (p % 4) for 32-unit rows, 8 ((p / 2) % 2) for 16-unit rows
- * and 0 for shorter rows.  Both orders keep each lane's tensor-core operand loads in
- * distinct shared-memory banks.  Capacity must be a multiple of 64 (the decode kernel
- * moves whole 64-token tiles).  Groups are 32 contiguous channels: original channels for the
- * reference, rotated channels for residuals.
+ * are stored in token pairs: in pair p (tokens 2p, 2p+1 of the tile) the 32-bit word at
+ * position u ^ swz(p) holds 16-bit unit u of token 2p's natural row (low half) and of token
+ * 2p+1's (high half), with swz(p) = 8 (p % 4) for 32-unit rows, 8 ((p / 2) % 2) for 16-unit
+ * rows and 0 for shorter rows.  Both orders keep each lane's tensor-core operand loads in
+ * distinct shared-memory banks.  Capacity must be a multiple of 64.  Groups are 32
+ * contiguous channels: original channels for the reference, rotated channels for residuals.
  */
 #ifndef RQ_H_
 #define RQ_H_
@@ -78,17 +90,16 @@ typedef struct {
 } rq_shape;
 
 typedef struct {
-  uint8_t* ref_codes[2];
-  uint16_t* ref_meta[2];
-  uint8_t* res_codes[2][RQ_MAX_LOOPS];
-  uint16_t* res_meta[2][RQ_MAX_LOOPS];
-  uint16_t* alpha[2][RQ_MAX_LOOPS];
-  const int8_t* rot_signs[2];
+  uint8_t* data;                /* the tile records (layout above), 256-byte aligned     */
+  const int8_t* rot_signs[2];   /* [Hkv][d] per K / V                                    */
 } rq_cache;
 
-/* Bytes of one layer's packed cache (K and V, all arrays above except rot_signs):
- * per token-head and K/V, d/2 + 4*ng for the reference plus d*b_l/8 + 4*ng + 2 per
- * non-final loop.  Returns 0 for an invalid shape. */
+/* Bytes of one tile record of this shape: 64 x the token-head bytes (0 if invalid). */
+size_t rq_record_bytes(const rq_shape* shape);
+
+/* Bytes of one layer's packed cache (all tile records, not rot_signs): per token-head and
+ * K/V, d/2 + 4*ng for the reference plus d*b_l/8 + 4*ng + 2 per non-final loop, times
+ * B * Hkv * capacity.  Returns 0 for an invalid shape. */
 size_t rq_cache_bytes(const rq_shape* shape);
 
 /* Deferred write (rit.work summary, "How each pass's KV cache is reconstructed": the
@@ -158,14 +169,9 @@ rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k,
 
 /* Paged cache (rit.work summary, "When ResidualQuant changes the infrastructure plan": the
  * pages' integration keeps the serving engine's paged KV cache; this is its block-table
- * form).  A page holds 64 consecutive tokens of one sequence for every kv-head.  In paged
- * mode every array of rq_cache except rot_signs is laid out per page instead of per
- * sequence:
- *   ref_codes[kv] uint8 [n_pages][Hkv][64][d/2], ref_meta[kv] fp16 [n_pages][Hkv][64][ng][2],
- *   res_codes[kv][l] uint8 [n_pages][Hkv][64][d*b_l/8], res_meta[kv][l] fp16
- *   [n_pages][Hkv][64][ng][2], alpha[kv][l] fp16 [n_pages][Hkv][64],
- * with the same row formats as above (V token pairs and their swizzle follow the token's
- * position within its page).  Tokens 64j..64j+63 of sequence b live in physical page
+ * form).  A page holds 64 consecutive tokens of one sequence for every kv-head: in paged
+ * mode the tile records are [n_pages][Hkv] instead of [B][Hkv][cap/64], each the same record
+ * as above.  Tokens 64j..64j+63 of sequence b live in physical page
  * block_table[b * max_pages + j].  shape->capacity must equal 64 * max_pages (the logical
  * capacity of a sequence).  The table is read on the device: an entry outside
  * [0, n_pages) is never dereferenced -- the encode skips that token, the decode reads page 0
@@ -173,7 +179,7 @@ rq_status rq_bf16_decode_attention(const rq_shape* shape, const uint16_t* k,
 typedef struct {
   const int32_t* block_table;  /* device int32 [B][max_pages]                         */
   int32_t max_pages;           /* table columns: logical pages per sequence            */
-  int32_t n_pages;             /* physical pages in each array                         */
+  int32_t n_pages;             /* physical pages (records per kv-head)                 */
 } rq_paging;
 
 /* Bytes of one layer's paged cache with n_pages physical pages (0 for an invalid shape). */

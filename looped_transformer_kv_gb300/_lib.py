@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librq.so")
 STATUS = {0: "RQ_OK", 1: "RQ_ERR_INVALID_ARG", 2: "RQ_ERR_UNSUPPORTED",
           3: "RQ_ERR_WORKSPACE", 4: "RQ_ERR_CUDA", 5: "RQ_ERR_INTERNAL"}
 
-EXPORTS = ("rq_cache_bytes", "rq_encode_append", "rq_decode_workspace_bytes",
+EXPORTS = ("rq_cache_bytes", "rq_record_bytes", "rq_encode_append", "rq_decode_workspace_bytes",
            "rq_decode_attention", "rq_bf16_decode_attention", "rq_status_str",
            "rq_synth_states", "rq_synth_queries", "rq_decode_noalloc_scratch_bytes",
            "rq_decode_attention_noalloc", "rq_paged_cache_bytes", "rq_paged_encode_append",
@@ -34,9 +34,7 @@ _P = ctypes.c_void_p
 
 
 class RqCache(ctypes.Structure):
-    _fields_ = [("ref_codes", _P * 2), ("ref_meta", _P * 2),
-                ("res_codes", (_P * RQ_MAX_LOOPS) * 2), ("res_meta", (_P * RQ_MAX_LOOPS) * 2),
-                ("alpha", (_P * RQ_MAX_LOOPS) * 2), ("rot_signs", _P * 2)]
+    _fields_ = [("data", _P), ("rot_signs", _P * 2)]
 
 
 class RqPaging(ctypes.Structure):
@@ -73,6 +71,8 @@ def lib():
     S, C = ctypes.POINTER(RqShape), ctypes.POINTER(RqCache)
     L.rq_cache_bytes.argtypes = [S]
     L.rq_cache_bytes.restype = sz
+    L.rq_record_bytes.argtypes = [S]
+    L.rq_record_bytes.restype = sz
     L.rq_encode_append.argtypes = [S, C, _P, ctypes.POINTER(i64), _P, i32, i32, _P]
     L.rq_encode_append.restype = i32
     L.rq_decode_workspace_bytes.argtypes = [S, i32, i32]

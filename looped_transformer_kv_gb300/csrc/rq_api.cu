@@ -36,13 +36,11 @@ rq_status check_shape(const rq_shape* s) {
 }
 
 rq_status check_cache(const rq_shape* s, const rq_cache* c) {
-  if (!c) return RQ_ERR_INVALID_ARG;
-  for (int kv = 0; kv < 2; ++kv) {
-    if (!c->ref_codes[kv] || !c->ref_meta[kv] || !c->rot_signs[kv]) return RQ_ERR_INVALID_ARG;
-    for (int l = 0; l < s->n_loops - 1; ++l)
-      if (!c->res_codes[kv][l] || !c->res_meta[kv][l] || !c->alpha[kv][l])
-        return RQ_ERR_INVALID_ARG;
-  }
+  (void)s;
+  if (!c || !c->data || !c->rot_signs[0] || !c->rot_signs[1]) return RQ_ERR_INVALID_ARG;
+  // every piece of a record a stage copies starts at a multiple of 128 bytes of its record,
+  // and records are a multiple of 128 bytes long: 16-byte alignment of the base suffices
+  if ((reinterpret_cast<uintptr_t>(c->data) & 15) != 0) return RQ_ERR_INVALID_ARG;
   return RQ_OK;
 }
 
@@ -155,6 +153,11 @@ extern "C" {
 size_t rq_cache_bytes(const rq_shape* s) {
   if (check_shape(s) != RQ_OK) return 0;
   return token_head_bytes(s) * size_t(s->capacity) * size_t(s->n_kv_heads) * size_t(s->batch);
+}
+
+size_t rq_record_bytes(const rq_shape* s) {
+  if (check_shape(s) != RQ_OK) return 0;
+  return size_t(rq::record_bytes(*s));
 }
 
 size_t rq_paged_cache_bytes(const rq_shape* s, int32_t n_pages) {

@@ -67,10 +67,10 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
   MmaArgs& a = bl.a;
   memset(&a, 0, sizeof(a));
   const int D = s.head_dim, NG = D / 32;
-  a.kc = cache.ref_codes[0];
-  a.km = cache.ref_meta[0];
-  a.vc = cache.ref_codes[1];
-  a.vm = cache.ref_meta[1];
+  a.data = cache.data;
+  a.rec_bytes = record_bytes(s);
+  // stage layout: the record's reference section, then the sections of the block's residual
+  // loops (consecutive loops, consecutive sections), the same offsets as in the record
   int off = 0;
   a.off_kc = off; off += kT * D / 2;
   a.off_km = off; off += kT * NG * 4;
@@ -82,12 +82,6 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
     const int bits = s.res_bits[l];
     res4 |= bits == 4;
     a.rbits[ri] = bits;
-    a.krc[ri] = cache.res_codes[0][l];
-    a.krm[ri] = cache.res_meta[0][l];
-    a.ka[ri] = cache.alpha[0][l];
-    a.vrc[ri] = cache.res_codes[1][l];
-    a.vrm[ri] = cache.res_meta[1][l];
-    a.va[ri] = cache.alpha[1][l];
     a.off_krc[ri] = off; off += kT * D * bits / 8;
     a.off_krm[ri] = off; off += kT * NG * 4;
     a.off_ka[ri] = off;  off += kT * 2;
@@ -96,6 +90,19 @@ bool build_block(const rq_shape& s, const rq_cache& cache, const QueryBlock& bq,
     a.off_va[ri] = off;  off += kT * 2;
   }
   a.stage_bytes = off;
+  const int refb = ref_section_bytes(D);
+  a.cp_src[0] = 0;
+  a.cp_dst[0] = 0;
+  if (bq.nr == 0 || bq.r0 == 0) {   // the reference section (and loops 0 ..): one piece
+    a.ncp = 1;
+    a.cp_bytes[0] = off;
+  } else {
+    a.ncp = 2;
+    a.cp_bytes[0] = refb;
+    a.cp_src[1] = loop_section_offset(D, s.res_bits, bq.r0);
+    a.cp_dst[1] = refb;
+    a.cp_bytes[1] = off - refb;
+  }
   a.qrm_bytes = masked_fragment_bytes(D, res4, bq.nr, block_packing(bq));
   a.blk = bq;
   a.n_pg = n_pg;
@@ -266,26 +273,40 @@ cudaError_t launch_rq_ablation_decode(const rq_shape& s, const rq_cache& cache, 
   const int bits = s.res_bits[loop];
   MmaArgs a;
   memset(&a, 0, sizeof(a));
-  a.kc = cache.ref_codes[0];
-  a.km = cache.ref_meta[0];
-  a.vc = cache.ref_codes[1];
-  a.vm = cache.ref_meta[1];
+  a.data = cache.data;
+  a.rec_bytes = record_bytes(s);
+  const int refb = ref_section_bytes(D);
+  const int rb = D * bits / 8;
   int off = 0;
-  if (mode != 2) {
+  if (mode != 2) {   // the reference section (mode 1: the a rows come along, unread)
     a.off_kc = off; off += kT * D / 2;
     a.off_km = off; off += kT * NG * 4;
     a.off_vc = off; off += kT * D / 2;
     a.off_vm = off; off += kT * NG * 4;
   }
   a.rbits[0] = bits;
-  a.krc[0] = cache.res_codes[0][loop];
-  a.krm[0] = cache.res_meta[0][loop];
-  a.vrc[0] = cache.res_codes[1][loop];
-  a.vrm[0] = cache.res_meta[1][loop];
-  a.off_krc[0] = off; off += kT * D * bits / 8;
+  a.off_krc[0] = off; off += kT * rb;
   a.off_krm[0] = off; off += kT * NG * 4;
-  a.off_vrc[0] = off; off += kT * D * bits / 8;
+  a.off_ka[0] = off;  off += kT * 2;
+  a.off_vrc[0] = off; off += kT * rb;
   a.off_vrm[0] = off; off += kT * NG * 4;
+  a.off_va[0] = off;  off += kT * 2;
+  const int secoff = loop_section_offset(D, s.res_bits, loop);
+  if (mode == 2) {            // the loop's section alone
+    a.ncp = 1;
+    a.cp_src[0] = secoff;
+    a.cp_dst[0] = 0;
+    a.cp_bytes[0] = off;
+  } else if (loop == 0) {     // reference and loop 0: one piece
+    a.ncp = 1;
+    a.cp_bytes[0] = off;
+  } else {
+    a.ncp = 2;
+    a.cp_bytes[0] = refb;
+    a.cp_src[1] = secoff;
+    a.cp_dst[1] = refb;
+    a.cp_bytes[1] = off - refb;
+  }
   a.stage_bytes = off;
   a.qrm_bytes = 0;
   QueryBlock bq;

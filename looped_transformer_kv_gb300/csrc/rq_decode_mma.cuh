@@ -53,16 +53,10 @@ constexpr int kIssuedSlot = 15;               // release-counter word holding th
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct MmaArgs {
-  const uint8_t* kc;
-  const uint16_t* km;
-  const uint8_t* vc;
-  const uint16_t* vm;
-  const uint8_t* krc[kMaxResPerBlock];
-  const uint16_t* krm[kMaxResPerBlock];
-  const uint16_t* ka[kMaxResPerBlock];
-  const uint8_t* vrc[kMaxResPerBlock];
-  const uint16_t* vrm[kMaxResPerBlock];
-  const uint16_t* va[kMaxResPerBlock];
+  const uint8_t* data;       // tile records of the packed cache
+  int64_t rec_bytes;         // bytes of one record
+  int ncp;                   // pieces of a record a stage takes (1 or 2): source offset in
+  int cp_src[2], cp_dst[2], cp_bytes[2];   // the record, offset in the stage, bytes
   int rbits[kMaxResPerBlock];
   const int8_t* ksigns;
   const uint16_t* q;
@@ -219,8 +213,9 @@ __device__ __forceinline__ void weights_to_b_packed(float w00, float w01, float 
 // Blocks of the final loop alone (NRT 0) and single-column blocks with a 2-bit residual loop
 // are held to 128 registers for four resident CTAs per SM; the others take up to 168 for three.
 // MODE (ablation rows of the method's steps; single-column blocks of one residual loop only):
-// 0 = the method; 1 = a fixed at 1 (no a stream is read); 2 = direct quantisation of the loop
-// (no reference is read: the score and the value are the loop's own codes alone, a = 0).
+// 0 = the method; 1 = a fixed at 1 (the a rows are not read); 2 = direct quantisation of the
+// loop (the reference is neither copied nor read: the score and the value are the loop's own
+// codes alone, a = 0).
 template <int D, bool RES4, int NRT, bool PAGED, int PK, int MODE = 0>
 __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 : 3) rq_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NG = D / 32;
@@ -249,7 +244,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   // residual loop K codes, K steps, K a, V codes, V steps, V a.  Fixed at compile time when
   // the residual-loop count is and every residual loop is 2-bit (for up to two residual
   // loops: with three, the constant addresses cost more registers than they save).
-  constexpr bool FIXED = MODE == 0 && !RES4 && NRT >= 0 && NRT <= 2;
+  constexpr bool FIXED = MODE != 2 && !RES4 && NRT >= 0 && NRT <= 2;
   constexpr int F_KM = kT * RB4, F_VC = F_KM + kT * NG * 4, F_VM = F_VC + kT * RB4;
   constexpr int F_RES = F_VM + kT * NG * 4;
   constexpr int F_KRM = kT * RB2, F_KA = F_KRM + kT * NG * 4, F_VRC = F_KA + kT * 2;
@@ -360,31 +355,19 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
     fence_mbar_init();
   }
 
+  // A stage is one or two contiguous pieces of the tile's record (the reference section and
+  // the sections of the block's residual loops), one bulk copy each.
   auto issue = [&](int tile) {
     if (a.withhold_first_tile && tile == 0) return;   // (test hook: the wait can only run out)
     const int st = tile % S;
     const uint32_t bar = smem_u32(&bars[st]);
     const uint32_t dst = smem_u32(smem + st * a.stage_bytes);
-    const int64_t tok = paged ? (int64_t(pid[tile]) * a.H + h) * kT
-                              : slot * a.cap + t_begin + int64_t(tile) * kT;
+    const int64_t rec = paged ? int64_t(pid[tile]) * a.H + h
+                              : slot * (a.cap / kT) + t_begin / kT + tile;
+    const uint8_t* src = a.data + rec * a.rec_bytes;
     mbar_arrive_expect_tx(bar, uint32_t(a.stage_bytes));
-    if constexpr (MODE != 2) {
-      bulk_g2s(dst + a.off_kc, a.kc + tok * RB4, kT * RB4, bar);
-      bulk_g2s(dst + a.off_km, a.km + tok * NG * 2, kT * NG * 4, bar);
-      bulk_g2s(dst + a.off_vc, a.vc + tok * RB4, kT * RB4, bar);
-      bulk_g2s(dst + a.off_vm, a.vm + tok * NG * 2, kT * NG * 4, bar);
-    }
-#pragma unroll
-    for (int ri = 0; ri < kMaxResPerBlock; ++ri) {
-      if (ri >= nr) break;
-      const int rb = (!RES4 || a.rbits[ri] == 2) ? RB2 : RB4;
-      bulk_g2s(dst + a.off_krc[ri], a.krc[ri] + tok * rb, kT * rb, bar);
-      bulk_g2s(dst + a.off_krm[ri], a.krm[ri] + tok * NG * 2, kT * NG * 4, bar);
-      if (MODE == 0) bulk_g2s(dst + a.off_ka[ri], a.ka[ri] + tok, kT * 2, bar);
-      bulk_g2s(dst + a.off_vrc[ri], a.vrc[ri] + tok * rb, kT * rb, bar);
-      bulk_g2s(dst + a.off_vrm[ri], a.vrm[ri] + tok * NG * 2, kT * NG * 4, bar);
-      if (MODE == 0) bulk_g2s(dst + a.off_va[ri], a.va[ri] + tok, kT * 2, bar);
-    }
+    bulk_g2s(dst + a.cp_dst[0], src + a.cp_src[0], uint32_t(a.cp_bytes[0]), bar);
+    if (a.ncp > 1) bulk_g2s(dst + a.cp_dst[1], src + a.cp_src[1], uint32_t(a.cp_bytes[1]), bar);
   };
   if (threadIdx.x == 0) {   // the barriers' initialisation is ordered before by the fence
     const int n0 = S < ntiles ? S : ntiles;

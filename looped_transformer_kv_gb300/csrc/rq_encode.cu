@@ -12,7 +12,9 @@ namespace rq {
 namespace {
 
 struct EncodeArgs {
-  rq_cache cache;
+  uint8_t* data;         // tile records of the packed cache
+  int64_t rec_bytes;     // bytes of one record
+  const int8_t* rot_signs[2];
   const uint16_t* kv_new;
   int64_t sb, st, skv, sl, sh;  // element strides of kv_new
   const int32_t* positions;
@@ -135,19 +137,19 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
   const int pos = a.positions ? a.positions[int64_t(b) * a.n_new + j] : a.pos_begin + j;
   if (pos < 0 || pos >= a.cap) return;
   const bool is_v = kv == 1;
-  // token rows of this (sequence, kv-head) start at row `base` of every array; the token is
-  // row base + tok.  Paged: the 64-token page holding the position, through the block table.
-  int64_t base;
-  int64_t tok;
+  // the tile record holding the token (contiguous: record (b, h, pos / 64); paged: the
+  // record of (page, h) of the 64-token page through the block table); the token is row
+  // tok = pos % 64 of each of its sections
+  int64_t rec_index;
   if (a.bt) {
     const int pg = a.bt[int64_t(b) * a.max_pages + (pos >> 6)];
     if (pg < 0 || pg >= a.n_pages) return;
-    base = (int64_t(pg) * a.H + h) * 64;
-    tok = pos & 63;
+    rec_index = int64_t(pg) * a.H + h;
   } else {
-    base = (int64_t(b) * a.H + h) * a.cap;
-    tok = pos;
+    rec_index = (int64_t(b) * a.H + h) * (a.cap / kTile) + (pos >> 6);
   }
+  uint8_t* const rec = a.data + rec_index * a.rec_bytes;
+  const int64_t tok = pos & 63;
 
   const uint16_t* src = a.kv_new + int64_t(b) * a.sb + int64_t(j) * a.st + int64_t(kv) * a.skv +
                         int64_t(h) * a.sh + hl * P;
@@ -186,11 +188,12 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
   uint16_t s_bits, z_bits;
   quantize_lane<P, 15>(x_ref, c, ref_hat, s_bits, z_bits);
   {
-    uint8_t* codes = a.cache.ref_codes[kv] + base * (D / 2);
+    // reference section: K codes, K meta, V codes, V meta (64 rows each)
+    uint8_t* codes = rec + kv * (kTile * (D / 2) + kTile * NG * 4);
     store_codes<P, 4, NG>(codes, tok, D / 2, is_v, c, hl);
     if (hl % LPG == 0) {
       const int g = hl / LPG;
-      uint16_t* meta = a.cache.ref_meta[kv] + (base + tok) * (2 * NG) + 2 * g;
+      uint8_t* meta = codes + kTile * (D / 2) + tok * (NG * 4) + g * 4;
       *reinterpret_cast<uint32_t*>(meta) = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
     }
   }
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
 
   float sgn[P];
   {
-    const int8_t* sp = a.cache.rot_signs[kv] + int64_t(h) * D + hl * P;
+    const int8_t* sp = a.rot_signs[kv] + int64_t(h) * D + hl * P;
 #pragma unroll
     for (int q = 0; q < P; ++q) sgn[q] = float(sp[q]);
   }
@@ -220,7 +223,13 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
     if (a.alpha_mode != 0) alpha = a.alpha_mode == 1 ? 1.f : 0.f;   // (ablation encodes)
     const uint16_t a_bits = float_to_half_bits(alpha);
     const float a_h = half_bits_to_float(a_bits);
-    if (hl == 0) a.cache.alpha[kv][l][base + tok] = a_bits;
+    // loop l's section: K codes, K meta, K a, V codes, V meta, V a (64 rows each)
+    const int bits = a.res_bits[l];
+    const int row = D * bits / 8;
+    uint8_t* const sec = rec + loop_section_offset(D, a.res_bits, l) +
+                         kv * (kTile * row + kTile * NG * 4 + kTile * 2);
+    if (hl == 0)
+      *reinterpret_cast<uint16_t*>(sec + kTile * row + kTile * NG * 4 + tok * 2) = a_bits;
     // residual, rotation R r = H (signs * r) / sqrt(d)
     float y[P];
 #pragma unroll
@@ -229,9 +238,7 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
 #pragma unroll
     for (int q = 0; q < P; ++q) y[q] *= inv_sqrt_d;
     float deq[P];
-    const int bits = a.res_bits[l];
-    const int row = D * bits / 8;
-    uint8_t* codes = a.cache.res_codes[kv][l] + base * row;
+    uint8_t* codes = sec;
     if (bits == 2) {
       quantize_lane<P, 3>(y, c, deq, s_bits, z_bits);
       store_codes<P, 2, NG>(codes, tok, row, is_v, c, hl);
@@ -241,7 +248,7 @@ __global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
     }
     if (hl % LPG == 0) {
       const int g = hl / LPG;
-      uint16_t* meta = a.cache.res_meta[kv][l] + (base + tok) * (2 * NG) + 2 * g;
+      uint8_t* meta = sec + kTile * row + tok * (NG * 4) + g * 4;
       *reinterpret_cast<uint32_t*>(meta) = uint32_t(s_bits) | (uint32_t(z_bits) << 16);
     }
   }
@@ -255,7 +262,10 @@ cudaError_t launch_encode(const rq_shape& s, const rq_cache& cache, const rq_pag
                           int32_t n_new, cudaStream_t stream, int alpha_mode) {
   EncodeArgs a;
   a.alpha_mode = alpha_mode;
-  a.cache = cache;
+  a.data = cache.data;
+  a.rec_bytes = record_bytes(s);
+  a.rot_signs[0] = cache.rot_signs[0];
+  a.rot_signs[1] = cache.rot_signs[1];
   a.kv_new = kv_new;
   a.sb = strides[0];
   a.st = strides[1];

@@ -9,6 +9,23 @@
 namespace rq {
 
 constexpr int kMaxResPerBlock = 8;   // residual loops handled by one decode launch
+constexpr int kTile = 64;            // tokens per tile record (and per decode stage)
+
+// Tile record of the packed cache (include/rq.h): 64-row sections, the reference section
+// (K codes, K meta, V codes, V meta) first, then one section per non-final loop (K codes,
+// K meta, K a, V codes, V meta, V a).  Byte sizes and offsets; every one a multiple of 128.
+__host__ __device__ inline int ref_section_bytes(int D) { return kTile * (D + 8 * (D / 32)); }
+__host__ __device__ inline int loop_section_bytes(int D, int bits) {
+  return kTile * (2 * (D * bits / 8) + 8 * (D / 32) + 4);
+}
+__host__ __device__ inline int loop_section_offset(int D, const int8_t* res_bits, int l) {
+  int o = ref_section_bytes(D);
+  for (int k = 0; k < l; ++k) o += loop_section_bytes(D, res_bits[k]);
+  return o;
+}
+inline int64_t record_bytes(const rq_shape& s) {
+  return loop_section_offset(s.head_dim, s.res_bits, s.n_loops - 1);
+}
 constexpr int kWsHeaderBytes = 256;  // workspace header: uint32 error word, then padding
 
 // Variants of the decode kernel that keep, per residual loop, the rotated-query fragments

@@ -43,50 +43,56 @@ PAGE = 64   # tokens per page of a paged cache
 
 
 class PackedCache:
-    """Device arrays of one layer's packed cache (layout of include/rq.h) + rotation signs.
-
-    With n_pages, the arrays are laid out per 64-token page ([n_pages][Hkv][64][...], the
-    paged form of include/rq.h) instead of per sequence ([B][Hkv][capacity][...])."""
+    """One layer's packed cache in device memory: the tile records of include/rq.h in one
+    buffer (256-byte aligned), [B][Hkv][capacity/64] records, or [n_pages][Hkv] in paged
+    form, plus the rotation signs.  record_bytes() is rq_record_bytes; section(...) gives the
+    byte range of one kind of row inside a record (for reading the cache back)."""
 
     def __init__(self, shape, rot_signs, device="cuda", n_pages=None):
         B, H, cap, d = shape.batch, shape.n_kv_heads, shape.capacity, shape.head_dim
         self.n_pages = n_pages
-        if n_pages is not None:
-            B, cap = n_pages, PAGE
-        ng = d // GROUP
-        u8, f16 = torch.uint8, torch.float16
         self.shape = shape
-        self.ref_codes = [torch.empty(B, H, cap, d // 2, dtype=u8, device=device) for _ in range(2)]
-        self.ref_meta = [torch.empty(B, H, cap, ng, 2, dtype=f16, device=device) for _ in range(2)]
-        self.res_codes = [[], []]
-        self.res_meta = [[], []]
-        self.alpha = [[], []]
-        for kv in range(2):
-            for b in res_bits_of(shape):
-                self.res_codes[kv].append(torch.empty(B, H, cap, d * b // 8, dtype=u8, device=device))
-                self.res_meta[kv].append(torch.empty(B, H, cap, ng, 2, dtype=f16, device=device))
-                self.alpha[kv].append(torch.empty(B, H, cap, dtype=f16, device=device))
+        self.rec = int(_lib.lib().rq_record_bytes(ctypes.byref(shape)))
+        assert self.rec > 0
+        n_rec = (n_pages * H) if n_pages is not None else (B * H * (cap // PAGE))
+        self.data = torch.empty(n_rec * self.rec, dtype=torch.uint8, device=device)
         self.rot_signs = rot_signs.to(device=device, dtype=torch.int8).contiguous()  # [2][H][d]
         assert tuple(self.rot_signs.shape) == (2, H, d)
         c = RqCache()
+        c.data = self.data.data_ptr()
         for kv in range(2):
-            c.ref_codes[kv] = self.ref_codes[kv].data_ptr()
-            c.ref_meta[kv] = self.ref_meta[kv].data_ptr()
             c.rot_signs[kv] = self.rot_signs[kv].data_ptr()
-            for l in range(shape.n_loops - 1):
-                c.res_codes[kv][l] = self.res_codes[kv][l].data_ptr()
-                c.res_meta[kv][l] = self.res_meta[kv][l].data_ptr()
-                c.alpha[kv][l] = self.alpha[kv][l].data_ptr()
         self.struct = c
 
+    def records(self):
+        """The records as [B][Hkv][capacity/64][rec] (or [n_pages][Hkv][rec] when paged)."""
+        s = self.shape
+        if self.n_pages is not None:
+            return self.data.view(self.n_pages, s.n_kv_heads, self.rec)
+        return self.data.view(s.batch, s.n_kv_heads, s.capacity // PAGE, self.rec)
+
+    def section(self, kind, kv, loop=None):
+        """(byte offset in a record, row bytes) of one kind of 64 rows: kind in 'codes',
+        'meta', 'alpha'; loop None = the reference section."""
+        d = self.shape.head_dim
+        ng = d // GROUP
+        if loop is None:
+            base = kv * PAGE * (d // 2 + 4 * ng)
+            return {"codes": (base, d // 2), "meta": (base + PAGE * d // 2, 4 * ng)}[kind]
+        bits = res_bits_of(self.shape)
+        off = PAGE * (d + 8 * ng)
+        for b in bits[:loop]:
+            off += PAGE * (2 * (d * b // 8) + 8 * ng + 4)
+        rb = d * bits[loop] // 8
+        base = off + kv * PAGE * (rb + 4 * ng + 2)
+        return {"codes": (base, rb), "meta": (base + PAGE * rb, 4 * ng),
+                "alpha": (base + PAGE * (rb + 4 * ng), 2)}[kind]
+
     def tensors(self):
-        out = list(self.ref_codes) + list(self.ref_meta)
-        for kv in range(2):
-            out += self.res_codes[kv] + self.res_meta[kv] + self.alpha[kv]
-        return out
+        return [self.data]
 
     def nbytes(self):
-        return sum(t.numel() * t.element_size() for t in self.tensors())
+        return self.data.numel()
 
 
 def cache_bytes(shape):

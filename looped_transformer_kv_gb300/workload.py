@@ -78,17 +78,13 @@ class Workload:
         del buf
 
     def _sub_cache(self, b0, nb):
-        """A view of the cache restricted to sequences [b0, b0+nb) (pointer offsets)."""
+        """A view of the cache restricted to sequences [b0, b0+nb) (a pointer offset: the
+        records of a sequence are contiguous)."""
         c = rq._lib.RqCache()
         full = self.cache
+        c.data = full.data.data_ptr() + b0 * self.H * (self.cap // rq.PAGE) * full.rec
         for kv in range(2):
-            c.ref_codes[kv] = full.ref_codes[kv][b0].data_ptr()
-            c.ref_meta[kv] = full.ref_meta[kv][b0].data_ptr()
             c.rot_signs[kv] = full.rot_signs[kv].data_ptr()
-            for l in range(self.L - 1):
-                c.res_codes[kv][l] = full.res_codes[kv][l][b0].data_ptr()
-                c.res_meta[kv][l] = full.res_meta[kv][l][b0].data_ptr()
-                c.alpha[kv][l] = full.alpha[kv][l][b0].data_ptr()
 
         class _V:
             pass
@@ -208,39 +204,41 @@ class Workload:
     def packed_slice_paged(self, pc, table, b, h, ntok):
         """packed_slice of a paged cache `pc` whose block table is `table` (host [B][pages])."""
         ntok += ntok % 2
-        out = {}
-        tb = table[b]
-        for kv in range(2):
-            out[("ref_codes", kv)] = _page_rows(pc.ref_codes[kv], tb, h, ntok).cpu().numpy()
-            out[("ref_meta", kv)] = _page_rows(pc.ref_meta[kv], tb, h, ntok).float().cpu().numpy()
-            for l in range(self.L - 1):
-                out[("res_codes", kv, l)] = _page_rows(pc.res_codes[kv][l], tb, h, ntok).cpu().numpy()
-                out[("res_meta", kv, l)] = _page_rows(pc.res_meta[kv][l], tb, h, ntok).float().cpu().numpy()
-                out[("alpha", kv, l)] = _page_rows(pc.alpha[kv][l], tb, h, ntok).float().cpu().numpy()
-        return out
+        npg = -(-ntok // rq.PAGE)
+        idx = torch.as_tensor(np.asarray(table[b][:npg], dtype=np.int64), device=pc.data.device)
+        return slice_from_records(pc, pc.records()[idx, h], ntok)
 
     def packed_slice(self, b, h, ntok):
         """Host copies of the packed arrays of (sequence b, kv-head h), tokens [0, ntok)."""
         ntok += ntok % 2
-        c = self.cache
-        out = {}
-        for kv in range(2):
-            out[("ref_codes", kv)] = c.ref_codes[kv][b, h, :ntok].cpu().numpy()
-            out[("ref_meta", kv)] = c.ref_meta[kv][b, h, :ntok].float().cpu().numpy()
-            for l in range(self.L - 1):
-                out[("res_codes", kv, l)] = c.res_codes[kv][l][b, h, :ntok].cpu().numpy()
-                out[("res_meta", kv, l)] = c.res_meta[kv][l][b, h, :ntok].float().cpu().numpy()
-                out[("alpha", kv, l)] = c.alpha[kv][l][b, h, :ntok].float().cpu().numpy()
-        return out
+        npg = -(-ntok // rq.PAGE)
+        return slice_from_records(self.cache, self.cache.records()[b, h, :npg], ntok)
 
 
-def _page_rows(arr, table_b, h, ntok):
-    """Rows [0, ntok) of one (sequence, kv-head) of a paged array [n_pages][Hkv][64][...],
-    following the sequence's block-table row `table_b` (host ints)."""
-    npg = -(-ntok // 64)
-    idx = torch.as_tensor(np.asarray(table_b[:npg], dtype=np.int64), device=arr.device)
-    rows = arr[idx, h]                                   # [npg][64][...]
-    return rows.reshape((npg * 64,) + tuple(rows.shape[2:]))[:ntok]
+def slice_from_records(pc, recs, ntok):
+    """The packed arrays of one (sequence, kv-head) of cache `pc` from its records [n][rec]
+    (uint8, on the device), tokens [0, ntok): each kind of row concatenated over the records
+    ({("ref_codes", kv): uint8 [ntok][row], ("ref_meta", kv): [ntok][ng][2], per loop l
+    ("res_codes", kv, l), ("res_meta", kv, l), ("alpha", kv, l): [ntok]}; fp16 as float32)."""
+    d, L = pc.shape.head_dim, pc.shape.n_loops
+    ng = d // rq.GROUP
+    out = {}
+
+    def rows(kind, kv, loop=None, dtype=None):
+        off, rb = pc.section(kind, kv, loop)
+        a = recs[:, off:off + rq.PAGE * rb].reshape(-1, rb)[:ntok]
+        if dtype is None:
+            return a.cpu().numpy()
+        return a.contiguous().view(dtype).float().cpu().numpy()
+
+    for kv in range(2):
+        out[("ref_codes", kv)] = rows("codes", kv)
+        out[("ref_meta", kv)] = rows("meta", kv, None, torch.float16).reshape(ntok, ng, 2)
+        for l in range(L - 1):
+            out[("res_codes", kv, l)] = rows("codes", kv, l)
+            out[("res_meta", kv, l)] = rows("meta", kv, l, torch.float16).reshape(ntok, ng, 2)
+            out[("alpha", kv, l)] = rows("alpha", kv, l, torch.float16).reshape(ntok)
+    return out
 
 
 def np_bf16(t):

@@ -54,6 +54,23 @@ def test_cache_bytes_closed_form(lib, d, L, bits):
     assert lib.lib().rq_cache_bytes(ctypes.byref(s)) == O.cache_bytes(d, L, bits, 64, 2, 2)
 
 
+@pytest.mark.parametrize("d,L,bits", [(128, 4, (2, 2, 2)), (64, 4, (4, 2, 2)), (128, 1, ())])
+def test_record_bytes_is_64_token_heads(lib, d, L, bits):
+    s = _shape(lib, head_dim=d, n_loops=L, res_bits=bits)
+    assert lib.lib().rq_record_bytes(ctypes.byref(s)) == O.cache_bytes(d, L, bits, 64)
+
+
+def test_misaligned_records_are_rejected(lib):
+    L = lib.lib()
+    s = _shape(lib)
+    c = lib.RqCache()
+    c.data = 256 + 8                                            # not 16-byte aligned
+    c.rot_signs[0] = c.rot_signs[1] = 16
+    p = ctypes.c_void_p(16)
+    assert L.rq_decode_attention(ctypes.byref(s), ctypes.byref(c), p, 0, 1, None, p, 64, p, p,
+                                 1 << 40, None) == 1
+
+
 def test_status_strings(lib):
     L = lib.lib()
     assert L.rq_status_str(0) == b"RQ_OK"
@@ -134,10 +151,8 @@ def test_noalloc_entry_point_returns_the_workspace_entry_points_status(lib, bad,
     L = lib.lib()
     s = _shape(lib, **bad)
     c = lib.RqCache()
-    for kv in range(2):                                         # non-null dummy arrays
-        c.ref_codes[kv] = c.ref_meta[kv] = c.rot_signs[kv] = 16
-        for l in range(16):
-            c.res_codes[kv][l] = c.res_meta[kv][l] = c.alpha[kv][l] = 16
+    c.data = 256                                                # non-null dummy records
+    c.rot_signs[0] = c.rot_signs[1] = 16
     p = ctypes.c_void_p(16)
     ws_status = L.rq_decode_attention(ctypes.byref(s), ctypes.byref(c), p, 0, 1, None, p, max_ctx,
                                       p, p, 1 << 40, None)

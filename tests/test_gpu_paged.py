@@ -42,17 +42,6 @@ def _paged_twin(w, spare_pages, seed):
     return pc, paging, bt, bt.cpu().numpy()
 
 
-def _arrays(cache):
-    out = [("ref_codes", kv, cache.ref_codes[kv]) for kv in range(2)]
-    out += [("ref_meta", kv, cache.ref_meta[kv]) for kv in range(2)]
-    for kv in range(2):
-        for l in range(len(cache.res_codes[kv])):
-            out += [("res_codes%d" % l, kv, cache.res_codes[kv][l]),
-                    ("res_meta%d" % l, kv, cache.res_meta[kv][l]),
-                    ("alpha%d" % l, kv, cache.alpha[kv][l])]
-    return out
-
-
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_paged_cache_matches_contiguous(case):
     name, over, ctx = CASES[case]
@@ -61,14 +50,13 @@ def test_paged_cache_matches_contiguous(case):
     w = Workload(cfg, capacity=cap, ctx_lens=ctx, batch=len(ctx))
     pc, paging, bt, table = _paged_twin(w, spare_pages=5, seed=case)
     torch.cuda.synchronize()
-    # every page byte for byte
-    for (name_a, kv, contig), (_, _, paged) in zip(_arrays(w.cache), _arrays(pc)):
-        c = contig.view(torch.uint8).reshape(w.B, w.H, cap // 64, 64, -1)
-        p = paged.view(torch.uint8).reshape(pc.n_pages, w.H, 64, -1)
-        for b in range(w.B):
-            got = p[torch.from_numpy(table[b]).long().cuda()]           # [pages][H][64][row]
-            want = c[b].permute(1, 0, 2, 3)                              # [pages][H][64][row]
-            assert torch.equal(got, want), (name_a, kv, b)
+    # every page's records byte for byte
+    c = w.cache.records()                                    # [B][H][pages][rec]
+    p = pc.records()                                         # [n_pages][H][rec]
+    for b in range(w.B):
+        got = p[torch.from_numpy(table[b]).long().cuda()]    # [pages][H][rec]
+        want = c[b].permute(1, 0, 2)                          # [pages][H][rec]
+        assert torch.equal(got, want), b
     # decode: all loops at once, each loop alone, a middle range
     calls = [(0, cfg.n_loops)] + [(l, 1) for l in range(cfg.n_loops)]
     if cfg.n_loops > 2:
@@ -107,18 +95,15 @@ def test_paged_table_entry_out_of_range_is_flagged_not_read():
     assert ws[:1].view(torch.int32).item() != 0
     assert torch.isnan(o.float()).all()
     # encode: the token whose page is out of range is skipped, the others are written
-    before = [t.clone() for (_, _, t) in _arrays(pc)]
+    before = pc.records().clone()
     kv = torch.zeros(1, 2, 2, L, w.H, w.d, dtype=torch.bfloat16, device="cuda")
     pos = torch.tensor([[70, 10]], dtype=torch.int32, device="cuda")   # page 1 (bad), page 0
     rqm.rq.paged_encode_append(w.shape, pc, bad_paging, kv, positions=pos)
     torch.cuda.synchronize()
-    after = [t for (_, _, t) in _arrays(pc)]
-    changed = [not torch.equal(x.view(torch.uint8), y.view(torch.uint8))
-               for x, y in zip(before, after)]
-    assert any(changed)                            # token 10 (page 0) was written
+    after = pc.records()
+    assert not torch.equal(before, after)          # token 10 (page 0) was written
     p1 = int(table[0, 1])
-    for x, y in zip(before, after):
-        assert torch.equal(x[p1].view(torch.uint8), y[p1].view(torch.uint8))
+    assert torch.equal(before[p1], after[p1])      # page 1's records untouched
 
 
 def test_bad_table_entry_in_single_column_calls_gives_nan():

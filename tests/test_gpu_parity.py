@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import looped_transformer_kv_gb300 as rqm
-    from looped_transformer_kv_gb300.workload import Workload
+    from looped_transformer_kv_gb300.workload import Workload, slice_from_records
 
 from rq_parity import check_slice, Follow, gpu_slice_to_oracle_names, packed_bytes_equal  # noqa: E402
 
@@ -97,14 +97,8 @@ def _encode_custom(x, d, L, res_bits, signs):
     kv = kv.reshape(1, N, 2, L, 1, d)
     rqm.encode_append(shape, cache, kv, pos_begin=0)
     torch.cuda.synchronize()
-    sl = {}                       # the N encoded slots (N even: whole V token pairs)
-    for k in range(2):
-        sl[("ref_codes", k)] = cache.ref_codes[k][0, 0, :N].cpu().numpy()
-        sl[("ref_meta", k)] = cache.ref_meta[k][0, 0, :N].float().cpu().numpy()
-        for l in range(L - 1):
-            sl[("res_codes", k, l)] = cache.res_codes[k][l][0, 0, :N].cpu().numpy()
-            sl[("res_meta", k, l)] = cache.res_meta[k][l][0, 0, :N].float().cpu().numpy()
-            sl[("alpha", k, l)] = cache.alpha[k][l][0, 0, :N].float().cpu().numpy()
+    # the N encoded slots (N even: whole V token pairs)
+    sl = slice_from_records(cache, cache.records()[0, 0, :cap // 64], N)
     return sl, cap
 
 

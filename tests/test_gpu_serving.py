@@ -22,13 +22,6 @@ if torch.cuda.is_available():
 from rq_parity import check_slice  # noqa: E402
 
 
-def _arrays(cache):
-    out = list(cache.ref_codes) + list(cache.ref_meta)
-    for kv in range(2):
-        out += cache.res_codes[kv] + cache.res_meta[kv] + cache.alpha[kv]
-    return out
-
-
 @pytest.mark.parametrize("name,over,ctx", [
     ("pr1_small", {}, [100]),
     ("layer_1p4b", dict(batch=2, n_q_heads=2, n_kv_heads=2), [130, 0]),
@@ -59,8 +52,7 @@ def test_graph_replayed_serving_steps_match_eager_steps(name, over, ctx):
         g.replay()
     torch.cuda.synchronize()
     assert ctx_g.tolist() == ctx_e.tolist() == [min(c + steps, cap) for c in ctx]
-    for a, b in zip(_arrays(w_graph.cache), _arrays(w_eager.cache)):
-        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    assert torch.equal(w_graph.cache.data, w_eager.cache.data)
     for a, b in zip(outs["g"], outs["e"]):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert wss["g"][:1].view(torch.int32).item() == 0

@@ -54,10 +54,8 @@ def test_noalloc_rejects_calls_beyond_its_scratch():
     shape = rq.make_shape(4096, 64, 64, 128, 16, 65536, (2,) * 15)
     assert rq.decode_workspace_bytes(shape, 16, 65536) > rq.noalloc_scratch_bytes()
     cache = rq._lib.RqCache()
-    for kv in range(2):                           # non-null dummies: the call must stop at the
-        cache.ref_codes[kv] = cache.ref_meta[kv] = cache.rot_signs[kv] = 16   # size check
-        for l in range(15):
-            cache.res_codes[kv][l] = cache.res_meta[kv][l] = cache.alpha[kv][l] = 16
+    cache.data = 256                              # non-null dummies: the call must stop at the
+    cache.rot_signs[0] = cache.rot_signs[1] = 16  # size check
     p = rq.ctypes.c_void_p(16)
     status = rq._lib.lib().rq_decode_attention_noalloc(
         rq.ctypes.byref(shape), rq.ctypes.byref(cache), p, 0, 16, None, p, 65536, p, None)
