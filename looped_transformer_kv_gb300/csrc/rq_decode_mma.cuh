@@ -240,11 +240,12 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   const QueryBlock blk = a.blk;
   const int nr = NRT >= 0 ? NRT : blk.nr;
 
-  // Stage layout (byte offsets within a stage): K codes, K steps, V codes, V steps, then per
-  // residual loop K codes, K steps, K a, V codes, V steps, V a.  Fixed at compile time when
-  // the residual-loop count is and every residual loop is 2-bit (for up to two residual
-  // loops: with three, the constant addresses cost more registers than they save).
-  constexpr bool FIXED = MODE != 2 && !RES4 && NRT >= 0 && NRT <= 2;
+  // Stage layout (byte offsets within a stage, the order of the cache's tile records): K
+  // codes, K steps, V codes, V steps, then per residual loop K codes, K steps, K a, V codes,
+  // V steps, V a.  Fixed at compile time when the residual-loop count is and every residual
+  // loop is 2-bit (the run-time offsets cost registers and constant-bank loads in the loop;
+  // 8-column blocks of three loops keep them: the constants spill there).
+  constexpr bool FIXED = MODE != 2 && !RES4 && NRT >= 0 && (NRT <= 2 || (NRT == 3 && PK == 1));
   constexpr int F_KM = kT * RB4, F_VC = F_KM + kT * NG * 4, F_VM = F_VC + kT * RB4;
   constexpr int F_RES = F_VM + kT * NG * 4;
   constexpr int F_KRM = kT * RB2, F_KA = F_KRM + kT * NG * 4, F_VRC = F_KA + kT * 2;
