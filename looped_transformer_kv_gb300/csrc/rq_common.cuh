@@ -62,10 +62,13 @@ __device__ __forceinline__ void warp_fwht(float (&v)[P], int lane) {
   }
 #pragma unroll
   for (int m = 1; m < LANES; m <<= 1) {
+    // the lane holding index bit m takes u - v, its partner v + u: one fused u + sign * v
+    // (sign * v is exact, so the result is the same single rounding)
+    const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
     for (int j = 0; j < P; ++j) {
-      float u = __shfl_xor_sync(RQ_FULL_MASK, v[j], m);
-      v[j] = (lane & m) ? (u - v[j]) : (v[j] + u);
+      const float u = __shfl_xor_sync(RQ_FULL_MASK, v[j], m);
+      v[j] = fmaf(sgn, v[j], u);
     }
   }
 }

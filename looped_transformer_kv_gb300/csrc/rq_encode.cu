@@ -117,7 +117,7 @@ __device__ __forceinline__ void store_codes(uint8_t* slot, int64_t tok, int row_
 }
 
 template <int D, int VL>
-__global__ void __launch_bounds__(128) encode_kernel(EncodeArgs a) {
+__global__ void __launch_bounds__(128, 8) encode_kernel(EncodeArgs a) {
   constexpr int P = D / VL;         // channels per lane
   constexpr int LPG = kGroup / P;   // lanes per 32-channel group
   constexpr int NG = D / kGroup;
