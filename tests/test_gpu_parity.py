@@ -85,6 +85,48 @@ def test_small_parity(case, pending):
     assert torch.allclose(per, outs[cfg.n_loops].float(), atol=2e-3, rtol=1e-2)
 
 
+# ------------------------------------------------------------------ seeded random shapes
+
+def _random_case(seed):
+    """A small shape drawn from the ranges the library supports (head dim 64/128, 1-8 query
+    heads per kv-head, 1-8 loops with 2- and 4-bit residual loops, ragged contexts), the
+    generator's parameters drawn as well; calls: every loop alone, all loops, a random range."""
+    rng = np.random.default_rng(1000 + seed)
+    d = int(rng.choice([64, 128]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    H = int(rng.integers(1, 4))
+    L = int(rng.integers(1, 9))
+    B = int(rng.integers(1, 4))
+    res_bits = tuple(int(rng.choice([2, 4])) for _ in range(L - 1))
+    sigma = tuple(float(np.float32(rng.uniform(0.03, 0.3))) for _ in range(L))
+    cfg = synth.Config(f"random{seed}", 1, B, g * H, H, d, L, 512, res_bits,
+                       int(rng.integers(0, 4)), float(rng.choice([4.0, 8.0, 16.0])), sigma,
+                       int(rng.integers(0, 2)), int(rng.integers(0, 1 << 20)))
+    ctx = [int(rng.choice([0, 1, 63, 64, 65, 128, 191, 257, 300, 384, 447])) for _ in range(B)]
+    lb = int(rng.integers(0, L))
+    lc = int(rng.integers(1, L - lb + 1))
+    return cfg, ctx, (lb, lc), bool(rng.integers(0, 2))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_shapes_parity(seed):
+    cfg, ctx, extra, pending = _random_case(seed)
+    w = Workload(cfg, capacity=max(ctx) + 2, ctx_lens=ctx, batch=len(ctx))
+    calls = [(l, 1) for l in range(cfg.n_loops)] + [(0, cfg.n_loops), extra]
+    outs, wss = [], []
+    for l0, lc in calls:
+        o, ws = w.out_buffer(lc), w.workspace(lc)
+        w.decode(l0, lc, o, ws, pending=pending)
+        outs.append(o)
+        wss.append(ws)
+    torch.cuda.synchronize()
+    for ws in wss:
+        assert ws[:1].view(torch.int32).item() == 0
+    for b in range(len(ctx)):
+        for h in range(cfg.n_kv_heads):
+            check_slice(w, b, h, calls, outs, pending=pending)
+
+
 # ------------------------------------------------------------------ degenerate inputs
 
 def _encode_custom(x, d, L, res_bits, signs):
