@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   constexpr bool SC = PK == 2;                      // one query column, groups in columns
   // 4-column packing with 2 or 3 residual loops of 2 bits: each loop's residual MMAs take the
   // rotated-query fragments masked to its columns (no per-loop accumulator to select from)
-  constexpr bool MASKB = PK == 1 && !RES4 && PER_LOOP && NRT >= 2;
+  constexpr bool MASKB = (PK == 1 || PK == 0) && !RES4 && PER_LOOP && NRT >= 2;
   static_assert(!SC || (NRT == 0 || NRT == 1) && D == 128, "single-column blocks: D 128, one loop");
   static_assert(MODE == 0 || (SC && NRT == 1 && !PAGED), "ablation modes: single-column, one loop");
   extern __shared__ __align__(128) uint8_t smem[];
@@ -526,13 +526,19 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
   }
   const int cw = c < NG ? c : 0;   // this lane's group in the offset MMAs' A operand
   // masked fragments: [ri][k-step][lane], the rotated-query fragment where the lane's column
-  // (high or low part of query column (lane / 4) & 3) is residual loop ri's, else zero
+  // (4-column packing: high or low part of query column (lane / 4) & 3; 8 columns: query
+  // column lane / 4, high and low parts) is residual loop ri's, else zero
   uint2* QRM = reinterpret_cast<uint2*>(smem + lay.qrm);
+  uint4* QRM4 = reinterpret_cast<uint4*>(smem + lay.qrm);
   if constexpr (MASKB) {
     for (int i = threadIdx.x; i < NRT * NG * 2 * 32; i += kW * 32) {
       const int ri = i / (NG * 2 * 32), rem = i % (NG * 2 * 32);
-      const uint2 v = *reinterpret_cast<const uint2*>(&QR2[rem]);
-      QRM[i] = col_ri(((rem & 31) >> 2) & 3) == ri ? v : make_uint2(0u, 0u);
+      if constexpr (HL) {
+        const uint2 v = *reinterpret_cast<const uint2*>(&QR2[rem]);
+        QRM[i] = col_ri(((rem & 31) >> 2) & 3) == ri ? v : make_uint2(0u, 0u);
+      } else {
+        QRM4[i] = col_ri((rem & 31) >> 2) == ri ? QR2[rem] : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
     __syncthreads();
   }
@@ -782,9 +788,13 @@ __global__ void __launch_bounds__(kW * 32, (NRT == 0 || (PK == 2 && !RES4)) ? 4 
                     a_pairs_4bit(wh, s, a1, a3);
                   }
                   const int fi = (gq * 2 + s) * 32 + lane;
-                  if constexpr (MASKB) {   // into the one accumulator: other loops' columns get 0
+                  if constexpr (MASKB && HL) {   // into the one accumulator: other loops' columns get 0
                     const uint2 bq = QRM[(ri * NG * 2 + gq * 2 + s) * 32 + lane];
                     mma_f16(dsel, a0, a1, a2, a3, bq.x, bq.y);
+                  } else if constexpr (MASKB) {
+                    const uint4 bq = QRM4[(ri * NG * 2 + gq * 2 + s) * 32 + lane];
+                    mma_f16(dsel, a0, a1, a2, a3, bq.x, bq.y);
+                    mma_f16(dsel, a0, a1, a2, a3, bq.z, bq.w);
                   } else if constexpr (HL) {
                     const uint2 bq = *reinterpret_cast<const uint2*>((RES4 && !two) ? &QR4[fi] : &QR2[fi]);
                     mma_f16(Dr, a0, a1, a2, a3, bq.x, bq.y);

@@ -29,12 +29,13 @@ inline int64_t record_bytes(const rq_shape& s) {
 constexpr int kWsHeaderBytes = 256;  // workspace header: uint32 error word, then padding
 
 // Variants of the decode kernel that keep, per residual loop, the rotated-query fragments
-// masked to the loop's columns (4-column packing, 2-bit residual loops, residual-loop count
-// fixed at compile time and >= 2): bytes of that region, else 0.  Kernel and host use this
-// one rule.
+// masked to the loop's columns (4- or 8-column packing, 2-bit residual loops, residual-loop
+// count fixed at compile time and >= 2): bytes of that region, else 0 (a lane's fragment is
+// 8 bytes with the 4-column packing, 16 -- high and low parts -- with 8 columns).  Kernel and
+// host use this one rule.
 __host__ __device__ inline int masked_fragment_bytes(int D, bool res4, int nr, int pk) {
   const bool fixed = (D == 128 && (nr == 2 || nr == 3)) || (D == 64 && nr == 3);
-  return (pk == 1 && !res4 && fixed) ? nr * (D / 32) * 2 * 32 * 8 : 0;
+  return ((pk == 1 || pk == 0) && !res4 && fixed) ? nr * (D / 32) * 2 * 32 * (pk == 0 ? 16 : 8) : 0;
 }
 
 // Packed-cache decode workspace: header, then one uint32 ticket per (sequence, kv-head, query
